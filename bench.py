@@ -1,0 +1,530 @@
+#!/usr/bin/env python
+"""Benchmark of the BitDelta hot path on GB300.
+
+Headline workload ("stack70b"): the seven linears (q, k, v, o, gate, up,
+down) of 20 decoder layers of a 70B-shaped model (hidden 8192, FFN 28672,
+8 key/value heads of 128) with a resident bf16 base (34.2 GB) and 14
+fine-tuned variants stored as BitDelta signs + scales (Laplace(0, 1e-3)
+deltas, 2.14 GB of bits each, all resident).  One step is one decode batch of
+128 tokens whose variant ids follow a Zipf(1.1) mix: the tokens are grouped
+by variant once, then every linear runs the fused multi-variant kernel
+y = x (W_base + alpha_v sign(delta_v))^T on its own synthetic activations.
+``value`` is tokens per second over all ranks (weak scaling: every rank is an
+independent replica; the path has no data exchange).
+
+The same run also times, on rank 0, the other steps of the path on their own
+workloads ("rows"): compression of 14 variants of a 28672 x 8192 matrix, the
+prefill linear (gate and up, 4 variants x 4096 tokens), and the single
+4096 x 4096 linear at 1..64 tokens.
+
+``--impl reference`` times the CPU oracle on a bounded sample of the same
+workload instead (host cores only).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "BitDelta fused linear: % HBM roofline (decode), % TC peak (prefill), tok/s"
+UNIT = "tok/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--path", default="auto", help="kernel path: auto|simt|decode_tc|prefill_tc")
+    p.add_argument("--layers", type=int, default=20)
+    p.add_argument("--tokens", type=int, default=128)
+    p.add_argument("--variants", type=int, default=14)
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--no-rows", action="store_true", help="skip the compress/prefill/single rows")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-sample-rows", type=int, default=192,
+                   help="rows per linear of one layer in the oracle's sample")
+    return p.parse_args()
+
+
+# -- helpers -------------------------------------------------------------------
+
+def peaks():
+    f = ROOT / "MEASURED_PEAKS.json"
+    if f.exists():
+        d = json.loads(f.read_text())
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def csrc_digest() -> str:
+    h = hashlib.sha256()
+    for p in sorted((ROOT / "bit_delta_compressed_gb300" / "csrc").glob("*")):
+        h.update(p.name.encode())
+        h.update(p.read_bytes())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_key: str):
+    """DRAM bytes per launch recorded from an ncu capture of the current
+    kernel sources (profiles/*.md lines 'traffic <key> <bytes> csrc <digest>'),
+    or None when absent or taken on older sources."""
+    digest = csrc_digest()
+    for f in sorted((ROOT / "profiles").glob("*.md")):
+        for line in f.read_text().splitlines():
+            m = re.match(r"\s*traffic\s+(\S+)\s+([0-9.eE+]+)\s+csrc\s+(\w+)", line)
+            if m and m.group(1) == kernel_key and m.group(3) == digest:
+                return float(m.group(2))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+
+    def start(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [s.strip() for s in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def gpu_uuid(torch, dev):
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+# -- the workload ----------------------------------------------------------------
+
+def distinct_count(ids) -> int:
+    return len(set(int(v) for v in ids))
+
+
+def build_stack(args, torch, bd, wl, dev, seed):
+    """Resident base weights, 14 variants' bits and scales, per-linear x."""
+    g = wl.generator(seed, dev)
+    V, M = args.variants, args.tokens
+    ids_cpu = wl.variant_ids_zipf(M, V, 1.1, wl.generator(seed + 1))
+    ids = ids_cpu.to(dev)
+    linears = []
+    for layer in range(args.layers):
+        for name, N, K in wl.LAYER_LINEARS:
+            wb = wl.base_weights(N, K, g, dev)
+            alphas = torch.empty(V, dtype=torch.float32, device=dev)
+            bits = []
+            ws = bd.compress_workspace(N, K, dev)
+            for v in range(V):
+                wf = wl.finetuned_weights(wb, 1e-3, g)
+                b = torch.empty((N, K // 32), dtype=torch.int32, device=dev)
+                bd.compress(wf, wb, workspace=ws, alpha_out=alphas[v:v + 1], bits_out=b)
+                bits.append(b)
+                del wf
+            x = wl.activations(M, K, g, dev)
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            linears.append({"name": "%d.%s" % (layer, name), "N": N, "K": K, "wb": wb,
+                            "alphas": alphas, "bits": bits, "ptrs": bd.bits_pointer_array(bits),
+                            "x": x, "y": y})
+    torch.cuda.synchronize()
+    return ids, ids_cpu, linears
+
+
+def linear_bytes(M, N, K, D, y_bytes=2):
+    """Algorithmic HBM bytes of one fused linear launch: the bf16 base once,
+    one bit per weight per distinct variant, activations in, outputs out."""
+    return 2 * N * K + D * N * K // 8 + 2 * M * K + y_bytes * M * N
+
+
+# -- CPU oracle sample -------------------------------------------------------------
+
+def oracle_sample_time(args, wl, rows_per_linear, seed):
+    """Time the oracle on one layer's seven linears, ``rows_per_linear`` output
+    rows each, all tokens; returns (seconds, weights covered, threads)."""
+    import numpy as np
+    import torch
+    import oracle
+    o = oracle.get()
+    g = wl.generator(seed + 7)
+    V, M = args.variants, args.tokens
+    ids = wl.variant_ids_zipf(M, V, 1.1, wl.generator(seed + 1)).numpy()
+    cases = []
+    for name, N, K in wl.LAYER_LINEARS:
+        r = min(rows_per_linear, N)
+        wb = wl.base_weights(r, K, g).view(torch.int16).numpy().view(np.uint16)
+        bits = [torch.randint(-2 ** 31, 2 ** 31, (r, K // 32), generator=g, dtype=torch.int64)
+                .to(torch.int32).numpy().view(np.uint32) for _ in range(V)]
+        alphas = np.full(V, 1e-3, dtype=np.float32)
+        x = wl.activations(M, K, g).view(torch.int16).numpy().view(np.uint16)
+        cases.append((x, wb, alphas, bits, r * K))
+    t0 = time.perf_counter()
+    for x, wb, alphas, bits, _ in cases:
+        o.linear(x, ids, wb, alphas, bits)
+    dt = time.perf_counter() - t0
+    return dt, sum(c[4] for c in cases), oracle.host_threads()
+
+
+def cpu_value(args, wl, seconds, weights_done):
+    total = args.layers * sum(n * k for _, n, k in wl.LAYER_LINEARS)
+    step_s = seconds * total / weights_done
+    return args.tokens / step_s
+
+
+# -- arms --------------------------------------------------------------------------
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import workloads as wl
+    for _ in range(args.warmup):
+        oracle_sample_time(args, wl, max(8, args.cpu_sample_rows // 8), args.seed)
+    times = []
+    weights = threads = 0
+    for _ in range(args.steps):
+        dt, weights, threads = oracle_sample_time(args, wl, max(8, args.cpu_sample_rows // 8), args.seed)
+        times.append(dt)
+    sec = sum(times) / len(times)
+    value = cpu_value(args, wl, sec, weights)
+    step_ms = args.tokens / value * 1e3
+    sample = ("oracle fp64 linear on layer 0's seven linears, %d output rows each, all %d tokens, "
+              "14 variants; step time extrapolated by weight count to %d layers"
+              % (max(8, args.cpu_sample_rows // 8), args.tokens, args.layers))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": stack_config(args, None),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def stack_config(args, D):
+    return {"workload": "stack70b", "layers": args.layers, "linears_per_layer": 7,
+            "hidden": 8192, "ffn": 28672, "kv_dim": 1024, "tokens": args.tokens,
+            "variants": args.variants, "variant_mix": "zipf(1.1)", "distinct_variants": D,
+            "laplace_b": 1e-3, "y_dtype": "bf16", "path": args.path,
+            "l2": "inputs larger than L2 (64 GB of weights and bits resident)"}
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import bit_delta_compressed_gb300 as bd
+    import workloads as wl
+
+    bd.get_lib()          # fails loudly if the library is missing
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    pk, pk_src = peaks()
+    seed = args.seed + 1000 * rank
+
+    ids, ids_cpu, linears = build_stack(args, torch, bd, wl, dev, seed)
+    V, M = args.variants, args.tokens
+    D = distinct_count(ids_cpu.tolist())
+    ws_bytes = max(int(bd.get_lib().bitdelta_linear_workspace(M, L["N"], L["K"], V)) for L in linears)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    n_lin = len(linears)
+
+    def new_event():
+        return torch.cuda.Event(enable_timing=True)
+    # one event pair around every fused-linear launch of every timed step
+    ev = [[(new_event(), new_event()) for _ in range(n_lin)] for _ in range(args.steps)]
+
+    def step(events=None):
+        bd.group(ids, V, ws)
+        for i, L in enumerate(linears):
+            if events is not None:
+                events[i][0].record(stream)
+            bd.linear_grouped(L["x"], L["wb"], L["alphas"], L["ptrs"], V, L["y"], ws, path=args.path)
+            if events is not None:
+                events[i][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = bd.device_status(ws)
+    if st != 0:
+        raise RuntimeError("device status after warm-up: " + bd.status_string(st))
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    sampler = ClockSampler(gpu_uuid(torch, dev)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    t0, t1 = new_event(), new_event()
+    t0.record(stream)
+    for s_i in range(args.steps):
+        step(ev[s_i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop() if sampler else None
+    ms_per_step = t0.elapsed_time(t1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms_per_step], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+    value = M * world / (ms_per_step / 1e3)
+
+    # roofline of the dominant kernel: algorithmic bytes per launch over the
+    # average launch duration inside the timed region
+    launch_ms = sum(a.elapsed_time(b) for row in ev for a, b in row) / (args.steps * n_lin)
+    alg = sum(linear_bytes(M, L["N"], L["K"], D) for L in linears) / n_lin
+    achieved = alg / (launch_ms / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / pk["hbm_gbs"], "traffic": profiled_traffic("linear_stack70b"),
+            "kernel": "fused multi-variant linear (%s path)" % args.path,
+            "alg_bytes_per_launch": alg, "avg_launch_us": launch_ms * 1e3,
+            "peak_source": ("measured: MEASURED_PEAKS.json hbm_gbs (copy)" if pk_src == "measured"
+                            else "fallback 6.8 TB/s")}
+
+    e2e = measure_e2e(args, torch, bd, linears, ids, ws, V, stream)
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; random-init 70B-shaped weights, Laplace deltas)",
+            "config": stack_config(args, D), "roofline": roof, "e2e": e2e,
+            "gpu_launches": (1 + n_lin) * args.steps, "clocks": clocks}
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        dt, w_done, threads = oracle_sample_time(args, wl, args.cpu_sample_rows, args.seed)
+        line["cpu_baseline"] = {
+            "value": cpu_value(args, wl, dt, w_done), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": "fp64 oracle linear on one layer's seven linears, %d output rows each, all %d "
+                      "tokens, 14 variants (%.1f s); extrapolated by weight count to %d layers"
+                      % (args.cpu_sample_rows, M, dt, args.layers)}
+    del linears
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_rows:
+        line["rows"] = run_rows(args, torch, bd, wl, dev, pk)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def measure_e2e(args, torch, bd, linears, ids, ws, V, stream):
+    """Same metric through the public API with host buffers: per step the
+    activations and ids go host->device from pinned memory and every y comes
+    back device->host, inside the timed region."""
+    hx = [L["x"].cpu().pin_memory() for L in linears]
+    hy = [torch.empty(L["y"].shape, dtype=L["y"].dtype, pin_memory=True) for L in linears]
+    hids = ids.cpu().pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in hx) + hids.numel() * 4
+    d2h = sum(t.numel() * t.element_size() for t in hy)
+
+    def e2e_step():
+        ids.copy_(hids, non_blocking=True)
+        for L, h in zip(linears, hx):
+            L["x"].copy_(h, non_blocking=True)
+        bd.group(ids, V, ws)
+        for L in linears:
+            bd.linear_grouped(L["x"], L["wb"], L["alphas"], L["ptrs"], V, L["y"], ws, path=args.path)
+        for L, h in zip(linears, hy):
+            h.copy_(L["y"], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    n = max(3, args.steps // 5)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / n
+    return {"value": args.tokens / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+def time_events(torch, fn, iters, stream):
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(iters):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / iters
+
+
+def run_rows(args, torch, bd, wl, dev, pk):
+    """Compress, prefill and the single-linear decode on their own workloads."""
+    stream = torch.cuda.current_stream()
+    rows = {}
+    # compress: 14 variants of one 28672 x 8192 bf16 matrix (inputs 6.6 GB)
+    g = wl.generator(args.seed + 50, dev)
+    N, K, V = 28672, 8192, 14
+    wb = wl.base_weights(N, K, g, dev)
+    wfs = [wl.finetuned_weights(wb, 1e-3, g) for _ in range(V)]
+    alphas = torch.empty(V, dtype=torch.float32, device=dev)
+    bits = [torch.empty((N, K // 32), dtype=torch.int32, device=dev) for _ in range(V)]
+    cws = bd.compress_workspace(N, K, dev)
+
+    def compress_all():
+        for v in range(V):
+            bd.compress(wfs[v], wb, workspace=cws, alpha_out=alphas[v:v + 1], bits_out=bits[v])
+    for _ in range(3):
+        compress_all()
+    ms = time_events(torch, compress_all, 5, stream)
+    cbytes = V * (2 * 2 * N * K + N * K // 8)
+    ach = cbytes / (ms / 1e3) / 1e9
+    rows["compress"] = {"workload": "14 variants of 28672x8192 bf16", "ms": ms,
+                        "roofline": {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
+                                     "unit": "GB/s", "frac": ach / pk["hbm_gbs"],
+                                     "traffic": profiled_traffic("compress_prefill14")}}
+    del wfs
+    torch.cuda.empty_cache()
+
+    # prefill: gate and up (28672 x 8192), 4 variants x 4096 tokens grouped
+    Vp, per = 4, 4096
+    ids = wl.variant_ids_blocks([per] * Vp).to(dev)
+    Mp = ids.numel()
+    mats = []
+    for _ in range(2):
+        w = wl.base_weights(N, K, g, dev)
+        b = [torch.randint(-2 ** 31, 2 ** 31, (N, K // 32), generator=g, device=dev,
+                           dtype=torch.int64).to(torch.int32) for _ in range(Vp)]
+        mats.append((w, b, bd.bits_pointer_array(b)))
+    al = torch.full((Vp,), 1e-3, device=dev)
+    x = wl.activations(Mp, K, g, dev)
+    y = torch.empty((Mp, N), dtype=torch.bfloat16, device=dev)
+    wsp = bd.linear_workspace(Mp, N, K, Vp, dev)
+    path = pick_path(bd, "prefill_tc" if args.path == "auto" else args.path,
+                     lambda p: bd.linear_grouped(x, mats[0][0], al, mats[0][2], Vp, y, wsp, path=p))
+
+    def prefill():
+        bd.group(ids, Vp, wsp)
+        for w, b, p in mats:
+            bd.linear_grouped(x, w, al, p, Vp, y, wsp, path=path)
+    prefill()
+    torch.cuda.synchronize()
+    ms = time_events(torch, prefill, 3, stream)
+    flops = 2 * 2 * Mp * N * K
+    tf = flops / (ms / 1e3) / 1e12
+    rows["prefill"] = {"workload": "gate+up 28672x8192, 4 variants x 4096 tokens", "ms": ms,
+                       "path": path,
+                       "roofline": {"bound": "tensor", "achieved": tf, "peak": pk["bf16_tflops"],
+                                    "unit": "TFLOP/s", "frac": tf / pk["bf16_tflops"],
+                                    "traffic": None}}
+    del mats, x, y
+    torch.cuda.empty_cache()
+
+    # single 4096 x 4096 linear, 1 variant, M in {1, 8, 32, 64}; enough weight
+    # copies rotate that every call reads from HBM (> 2x L2)
+    N = K = 4096
+    copies = 16
+    ws_list = []
+    for _ in range(copies):
+        w = wl.base_weights(N, K, g, dev)
+        b = torch.randint(-2 ** 31, 2 ** 31, (N, K // 32), generator=g, device=dev,
+                          dtype=torch.int64).to(torch.int32)
+        ws_list.append((w, b, bd.bits_pointer_array([b])))
+    al1 = torch.full((1,), 5e-4, device=dev)
+    single = {}
+    for M in (1, 8, 32, 64):
+        x = wl.activations(M, K, g, dev)
+        ids1 = torch.zeros(M, dtype=torch.int32, device=dev)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        wsm = bd.linear_workspace(M, N, K, 1, dev)
+        bd.group(ids1, 1, wsm)
+
+        def run_all():
+            for w, b, p in ws_list:
+                bd.linear_grouped(x, w, al1, p, 1, y, wsm, path=args.path)
+        run_all()
+        ms = time_events(torch, run_all, 10, stream) / copies
+        byt = linear_bytes(M, N, K, 1)
+        ach = byt / (ms / 1e3) / 1e9
+        single["M=%d" % M] = {"us": ms * 1e3, "achieved_gbs": ach, "frac": ach / pk["hbm_gbs"]}
+    rows["single4096"] = single
+    return rows
+
+
+def pick_path(bd, preferred, call):
+    """``preferred`` if the library takes it for this shape, else "auto"."""
+    try:
+        call(preferred)
+        return preferred
+    except bd.BitDeltaError as e:
+        if e.code != bd.BD_ERR_UNSUPPORTED:
+            raise
+        return "auto"
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,49 @@
+// bd_api.cu -- status handling and small shared host helpers of the C ABI.
+#include "bd_internal.cuh"
+
+namespace bd {
+
+int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+    int n = 1;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n < 1) n = 1;
+    if (dev >= 0 && dev < 64) cached[dev] = n;
+    return n;
+}
+
+}  // namespace bd
+
+extern "C" bd_status bitdelta_device_status(void* workspace, void* stream) {
+    if (!workspace) return BD_ERR_NULL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return BD_ERR_CUDA;
+    unsigned word = 0;
+    if (cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return BD_ERR_CUDA;
+    if (word != 0 && cudaMemset(workspace, 0, sizeof word) != cudaSuccess) return BD_ERR_CUDA;
+    for (unsigned c = 1; c < 32; ++c)
+        if (word & (1u << c)) return static_cast<bd_status>(c);
+    return BD_OK;
+}
+
+extern "C" const char* bitdelta_status_string(bd_status s) {
+    switch (s) {
+        case BD_OK: return "ok";
+        case BD_ERR_NULL: return "a required pointer is NULL";
+        case BD_ERR_ALIGN: return "a pointer is not suitably aligned";
+        case BD_ERR_SHAPE: return "invalid shape";
+        case BD_ERR_DTYPE: return "unsupported dtype";
+        case BD_ERR_VARIANT: return "variant id outside [-1, V)";
+        case BD_ERR_WORKSPACE: return "workspace missing or too small";
+        case BD_ERR_CUDA: return "CUDA runtime error";
+        case BD_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
+        case BD_ERR_UNSUPPORTED: return "kernel path does not support this shape";
+    }
+    return "unknown status";
+}
+
+extern "C" int bitdelta_abi_version(void) { return BITDELTA_ABI_VERSION; }

@@ -1,0 +1,69 @@
+// bd_internal.cuh -- helpers shared by the library's translation units.
+//
+// Workspace header (the first 256 bytes of every workspace):
+//   u32 [0]  status word: device-detected errors, OR-ed as (1 << bd_status)
+//   u32 [1]  compress: ticket of the last-block-done reduction
+//   u32 [2]  diagnostic: where a bounded wait gave up (0 = never)
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "bitdelta.h"
+
+namespace bd {
+
+constexpr size_t kHeaderBytes = 256;
+constexpr size_t kAlign = 256;
+
+__host__ __device__ inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Device-side error report into the workspace status word.
+__device__ __forceinline__ void report(unsigned* status, bd_status code) {
+    atomicOr(status, 1u << static_cast<unsigned>(code));
+}
+
+// bf16 bit patterns -> f32 (exact).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// 16-byte streaming load that skips L1 (data read exactly once).
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// Launch check: returns BD_ERR_CUDA if the last launch failed.
+inline bd_status launch_status() {
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
+}
+
+// ---- linear workspace layout (shared by the dispatcher and kernels) ----
+
+struct GroupView {
+    int32_t* counts;     // [V + 2]: bucket 0 = id -1 (base), 1..V = variants, V+1 = invalid
+    int32_t* offsets;    // [V + 3]: exclusive prefix of counts
+    int32_t* pos2tok;    // [M]: grouped position -> original token
+    int32_t* pos_var;    // [M]: grouped position -> variant id (-1 base, -2 invalid)
+};
+
+struct LinearWorkspace {
+    unsigned* status;
+    GroupView g;
+    void* tc_scratch;    // tensor-core paths: staged activations
+    size_t tc_bytes;
+    size_t total;
+};
+
+LinearWorkspace linear_workspace_layout(void* base, int64_t M, int64_t N, int64_t K, int32_t V);
+
+}  // namespace bd

@@ -1,0 +1,340 @@
+// bd_linear.cu -- the multi-variant fused linear: token grouping, the CUDA-core
+// kernel, and the dispatcher behind bitdelta_linear.
+//
+// Page: "BitDelta: serving 14 Zen models from one GPU cluster", section
+// "Serving architecture": variants share one resident base; a request's
+// effective weight W_eff = W_base + alpha_v * sign(delta_v) is rebuilt on the
+// fly inside the matmul kernel from the base weights and the packed delta
+// bits, and never written to HBM.  A batch here mixes tokens of different
+// variants; they are grouped by variant id so that each variant's bits are
+// read once per weight tile.
+//
+// Every path computes, per token t of variant v and output row n,
+//   y[t, n] = sum_k x[t,k] W_base[n,k]  +  alpha_v * sum_k x[t,k] s_v[n,k]
+// with fp32 accumulation, i.e. the base product and the sign product are kept
+// apart and combined with the f32 alpha in the epilogue.
+#include "bd_internal.cuh"
+#include "bd_paths.cuh"
+
+namespace bd {
+
+LinearWorkspace linear_workspace_layout(void* base, int64_t M, int64_t N, int64_t K, int32_t V) {
+    LinearWorkspace w{};
+    char* p = static_cast<char*>(base);
+    size_t off = 0;
+    w.status = reinterpret_cast<unsigned*>(p);
+    off += kHeaderBytes;
+    auto take = [&](size_t bytes) {
+        char* r = p ? p + off : nullptr;
+        off += round_up(bytes, kAlign);
+        return r;
+    };
+    const size_t m = static_cast<size_t>(M > 0 ? M : 0);
+    w.g.counts = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (V + 2)));
+    w.g.offsets = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (V + 3)));
+    w.g.pos2tok = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (m ? m : 1)));
+    w.g.pos_var = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (m ? m : 1)));
+    w.tc_bytes = tc_scratch_bytes(M, N, K, V);
+    w.tc_scratch = w.tc_bytes ? take(w.tc_bytes) : nullptr;
+    w.total = off;
+    return w;
+}
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// Token grouping: a stable counting sort of the tokens by variant id.
+// Bucket 0 holds id -1 (the base model), bucket 1 + v holds variant v, and the
+// last bucket collects ids outside [-1, V) (reported, output rows zeroed).
+// One block; tokens are placed 1024 at a time with warp match + ballots so the
+// order inside every bucket is the token order.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int bucket_of(int32_t id, int V) {
+    return (id >= -1 && id < V) ? id + 1 : V + 1;
+}
+
+__global__ void __launch_bounds__(1024) group_kernel(const int32_t* __restrict__ ids, int M, int V,
+                                                     GroupView g, unsigned* status) {
+    extern __shared__ int sm[];
+    const int nb = V + 2;
+    int* hist = sm;                    // [32][nb] per-warp counts of the current slice
+    int* total = hist + 32 * nb;       // [nb]
+    int* start = total + nb;           // [nb]
+    int* placed = start + nb;          // [nb]
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < nb; i += blockDim.x) { total[i] = 0; placed[i] = 0; }
+    __syncthreads();
+    bool bad = false;
+    for (int t = threadIdx.x; t < M; t += blockDim.x) {
+        const int b = bucket_of(ids[t], V);
+        bad |= (b == V + 1);
+        atomicAdd(&total[b], 1);
+    }
+    if (__syncthreads_or(bad) && threadIdx.x == 0) report(status, BD_ERR_VARIANT);
+    if (threadIdx.x == 0) {
+        int run = 0;
+        for (int b = 0; b < nb; ++b) {
+            start[b] = run;
+            g.offsets[b] = run;
+            g.counts[b] = total[b];
+            run += total[b];
+        }
+        g.offsets[nb] = run;
+    }
+    __syncthreads();
+    for (int s0 = 0; s0 < M; s0 += blockDim.x) {
+        const int t = s0 + threadIdx.x;
+        const int b = (t < M) ? bucket_of(ids[t], V) : -1;
+        for (int i = threadIdx.x; i < 32 * nb; i += blockDim.x) hist[i] = 0;
+        __syncthreads();
+        const unsigned peers = __match_any_sync(0xffffffffu, b);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        if (b >= 0 && rank == 0) hist[warp * nb + b] = __popc(peers);
+        __syncthreads();
+        if (b >= 0) {
+            int before = 0;
+            for (int w = 0; w < warp; ++w) before += hist[w * nb + b];
+            const int pos = start[b] + placed[b] + before + rank;
+            g.pos2tok[pos] = t;
+            g.pos_var[pos] = (b == V + 1) ? -2 : b - 1;
+        }
+        __syncthreads();
+        for (int bb = threadIdx.x; bb < nb; bb += blockDim.x) {
+            int sum = 0;
+            for (int w = 0; w < 32; ++w) sum += hist[w * nb + bb];
+            placed[bb] += sum;
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// CUDA-core path.  One warp per output row; lanes stride over 8-column chunks
+// of K (16-byte loads of W_base and x, one byte of bits per variant); tokens
+// are walked in grouped order, 8 at a time, with separate fp32 accumulators
+// for the base and sign products.
+// ---------------------------------------------------------------------------
+constexpr int kSimtWarps = 8;
+constexpr int kSimtTok = 8;
+
+__global__ void __launch_bounds__(kSimtWarps * 32)
+simt_linear_kernel(const uint4* __restrict__ x, const uint4* __restrict__ w_base,
+                   const float* __restrict__ alphas, BitsTable bt, int64_t M, int64_t N,
+                   int64_t K, GroupView g, void* y, int y_bf16) {
+    const int lane = threadIdx.x & 31;
+    const int64_t n = static_cast<int64_t>(blockIdx.x) * kSimtWarps + (threadIdx.x >> 5);
+    if (n >= N) return;
+    const int64_t kc = K / 8;                              // 8-column chunks per row
+    const uint4* wrow = w_base + n * kc;
+    for (int64_t p0 = 0; p0 < M; p0 += kSimtTok) {
+        int tok[kSimtTok], var[kSimtTok];
+#pragma unroll
+        for (int j = 0; j < kSimtTok; ++j) {
+            const int64_t p = p0 + j;
+            tok[j] = (p < M) ? g.pos2tok[p] : -1;
+            var[j] = (p < M) ? g.pos_var[p] : -2;
+        }
+        float accb[kSimtTok], accs[kSimtTok];
+#pragma unroll
+        for (int j = 0; j < kSimtTok; ++j) { accb[j] = 0.f; accs[j] = 0.f; }
+        for (int64_t c = lane; c < kc; c += 32) {
+            const uint4 wv = __ldg(wrow + c);
+            const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+            float wf[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) { wf[2 * i] = bf16_lo(ww[i]); wf[2 * i + 1] = bf16_hi(ww[i]); }
+#pragma unroll
+            for (int j = 0; j < kSimtTok; ++j) {
+                if (tok[j] < 0 || var[j] == -2) continue;
+                const uint4 xv = __ldg(x + static_cast<int64_t>(tok[j]) * kc + c);
+                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                float xf[8];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) { xf[2 * i] = bf16_lo(xw[i]); xf[2 * i + 1] = bf16_hi(xw[i]); }
+                float db = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) db = fmaf(xf[i], wf[i], db);
+                accb[j] += db;
+                if (var[j] >= 0) {
+                    const uint32_t byte = __ldg(bt.p[var[j]] + n * kc + c);
+                    float ds = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) ds += ((byte >> i) & 1u) ? xf[i] : -xf[i];
+                    accs[j] += ds;
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kSimtTok; ++j) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                accb[j] += __shfl_xor_sync(0xffffffffu, accb[j], o);
+                accs[j] += __shfl_xor_sync(0xffffffffu, accs[j], o);
+            }
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int j = 0; j < kSimtTok; ++j) {
+                if (tok[j] < 0) continue;
+                float out = 0.f;
+                if (var[j] >= 0) out = fmaf(alphas[var[j]], accs[j], accb[j]);
+                else if (var[j] == -1) out = accb[j];
+                const int64_t o = static_cast<int64_t>(tok[j]) * N + n;
+                if (y_bf16) static_cast<__nv_bfloat16*>(y)[o] = __float2bfloat16_rn(out);
+                else static_cast<float*>(y)[o] = out;
+            }
+        }
+    }
+}
+
+bd_status launch_group(const int32_t* ids, int64_t M, int32_t V, const LinearWorkspace& w,
+                       cudaStream_t s) {
+    int threads = static_cast<int>(round_up(static_cast<size_t>(M), 32));
+    if (threads > 1024) threads = 1024;
+    if (threads < 32) threads = 32;
+    const size_t smem = sizeof(int) * (32 * (V + 2) + 3 * (V + 2));
+    group_kernel<<<1, threads, smem, s>>>(ids, static_cast<int>(M), V, w.g, w.status);
+    return launch_status();
+}
+
+bd_status launch_simt(const LinearArgs& a, const LinearWorkspace& w, cudaStream_t s) {
+    const int64_t blocks = (a.N + kSimtWarps - 1) / kSimtWarps;
+    simt_linear_kernel<<<static_cast<unsigned>(blocks), kSimtWarps * 32, 0, s>>>(
+        static_cast<const uint4*>(a.x), static_cast<const uint4*>(a.w_base), a.alphas, a.bits,
+        a.M, a.N, a.K, w.g, a.y, a.y_dtype == BD_BF16);
+    return launch_status();
+}
+
+bd_status check_linear_args(const void* x, const int32_t* ids, int64_t M, int64_t N, int64_t K,
+                            const void* w_base, const float* alphas,
+                            const uint32_t* const* bits, int32_t V, const void* y,
+                            bd_dtype y_dtype) {
+    if (M < 0 || N < 1 || K < 32 || K % 32 != 0) return BD_ERR_SHAPE;
+    if (V < 0 || V > BITDELTA_MAX_VARIANTS) return BD_ERR_SHAPE;
+    if (M > (int64_t(1) << 30) || N > (int64_t(1) << 31) || K > (int64_t(1) << 31))
+        return BD_ERR_SHAPE;
+    if (y_dtype != BD_F32 && y_dtype != BD_BF16) return BD_ERR_DTYPE;
+    if (M == 0) return BD_OK;
+    if (!x || !ids || !w_base || !y) return BD_ERR_NULL;
+    if (V > 0 && (!alphas || !bits)) return BD_ERR_NULL;
+    for (int v = 0; v < V; ++v)
+        if (!bits[v]) return BD_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(w_base, 16) || !aligned(y, 16) || !aligned(ids, 4))
+        return BD_ERR_ALIGN;
+    if (V > 0 && !aligned(alphas, 4)) return BD_ERR_ALIGN;
+    for (int v = 0; v < V; ++v)
+        if (!aligned(bits[v], 16)) return BD_ERR_ALIGN;
+    return BD_OK;
+}
+
+}  // namespace
+}  // namespace bd
+
+using namespace bd;
+
+extern "C" size_t bitdelta_linear_workspace(int64_t M, int64_t N, int64_t K, int32_t V) {
+    if (M < 0 || N < 1 || K < 32 || K % 32 != 0 || V < 0 || V > BITDELTA_MAX_VARIANTS) return 0;
+    return linear_workspace_layout(nullptr, M, N, K, V).total;
+}
+
+namespace {
+
+bd_status prepare(const void* x, int64_t M, int64_t N, int64_t K, const void* w_base,
+                  const float* alphas, const uint32_t* const* bits, int32_t V, void* y,
+                  bd_dtype y_dtype, void* workspace, size_t ws_bytes, bd_path& path,
+                  LinearArgs& a, LinearWorkspace& w) {
+    if (!workspace) return BD_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return BD_ERR_ALIGN;
+    w = linear_workspace_layout(workspace, M, N, K, V);
+    if (ws_bytes < w.total) return BD_ERR_WORKSPACE;
+    a.x = x;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.w_base = w_base;
+    a.alphas = alphas;
+    a.V = V;
+    for (int v = 0; v < BITDELTA_MAX_VARIANTS; ++v)
+        a.bits.p[v] = (v < V) ? reinterpret_cast<const uint8_t*>(bits[v]) : nullptr;
+    a.bits_host = bits;
+    a.y = y;
+    a.y_dtype = y_dtype;
+    if (path == BD_PATH_AUTO) path = choose_path(a);
+    if (path != BD_PATH_SIMT && path != BD_PATH_DECODE_TC && path != BD_PATH_PREFILL_TC)
+        return BD_ERR_UNSUPPORTED;
+    if (path == BD_PATH_DECODE_TC && !decode_tc_supported(a)) return BD_ERR_UNSUPPORTED;
+    if (path == BD_PATH_PREFILL_TC && !prefill_tc_supported(a)) return BD_ERR_UNSUPPORTED;
+    return BD_OK;
+}
+
+bd_status launch_path(bd_path path, const LinearArgs& a, const LinearWorkspace& w,
+                      cudaStream_t s) {
+    switch (path) {
+        case BD_PATH_DECODE_TC: return launch_decode_tc(a, w, s);
+        case BD_PATH_PREFILL_TC: return launch_prefill_tc(a, w, s);
+        default: return launch_simt(a, w, s);
+    }
+}
+
+}  // namespace
+
+extern "C" bd_status bitdelta_group(const int32_t* variant_ids, int64_t M, int32_t V,
+                                    void* workspace, size_t ws_bytes, void* stream) {
+    if (M < 0 || M > (int64_t(1) << 30) || V < 0 || V > BITDELTA_MAX_VARIANTS) return BD_ERR_SHAPE;
+    if (M == 0) return BD_OK;
+    if (!variant_ids) return BD_ERR_NULL;
+    if (!aligned(variant_ids, 4)) return BD_ERR_ALIGN;
+    if (!workspace) return BD_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return BD_ERR_ALIGN;
+    LinearWorkspace w = linear_workspace_layout(workspace, M, 1, 32, V);
+    const size_t group_end = static_cast<size_t>(
+        reinterpret_cast<char*>(w.g.pos_var) - static_cast<char*>(workspace)) +
+        round_up(sizeof(int32_t) * static_cast<size_t>(M), kAlign);
+    if (ws_bytes < group_end) return BD_ERR_WORKSPACE;
+    return launch_group(variant_ids, M, V, w, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" bd_status bitdelta_linear_grouped(const void* x, int64_t M, int64_t N, int64_t K,
+                                             const void* w_base, const float* alphas,
+                                             const uint32_t* const* bits, int32_t V, void* y,
+                                             bd_dtype y_dtype, void* workspace, size_t ws_bytes,
+                                             void* stream, bd_path path) {
+    const int32_t one = 0;
+    bd_status st = check_linear_args(x, &one, M, N, K, w_base, alphas, bits, V, y, y_dtype);
+    if (st != BD_OK) return st;
+    if (M == 0) return BD_OK;
+    LinearArgs a;
+    LinearWorkspace w;
+    a.ids = nullptr;
+    st = prepare(x, M, N, K, w_base, alphas, bits, V, y, y_dtype, workspace, ws_bytes, path, a, w);
+    if (st != BD_OK) return st;
+    return launch_path(path, a, w, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" bd_status bitdelta_linear_ex(const void* x, const int32_t* variant_ids, int64_t M,
+                                        int64_t N, int64_t K, const void* w_base,
+                                        const float* alphas, const uint32_t* const* bits,
+                                        int32_t V, void* y, bd_dtype y_dtype, void* workspace,
+                                        size_t ws_bytes, void* stream, bd_path path) {
+    bd_status st = check_linear_args(x, variant_ids, M, N, K, w_base, alphas, bits, V, y, y_dtype);
+    if (st != BD_OK) return st;
+    if (M == 0) return BD_OK;
+    LinearArgs a;
+    LinearWorkspace w;
+    a.ids = variant_ids;
+    st = prepare(x, M, N, K, w_base, alphas, bits, V, y, y_dtype, workspace, ws_bytes, path, a, w);
+    if (st != BD_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    st = launch_group(variant_ids, M, V, w, s);
+    if (st != BD_OK) return st;
+    return launch_path(path, a, w, s);
+}
+
+extern "C" bd_status bitdelta_linear(const void* x, const int32_t* variant_ids, int64_t M,
+                                     int64_t N, int64_t K, const void* w_base,
+                                     const float* alphas, const uint32_t* const* bits, int32_t V,
+                                     void* y, bd_dtype y_dtype, void* workspace, size_t ws_bytes,
+                                     void* stream) {
+    return bitdelta_linear_ex(x, variant_ids, M, N, K, w_base, alphas, bits, V, y, y_dtype,
+                              workspace, ws_bytes, stream, BD_PATH_AUTO);
+}
