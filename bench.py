@@ -55,7 +55,7 @@ def parse_args():
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-rows", action="store_true", help="skip the compress/prefill/single rows")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--cpu-sample-rows", type=int, default=192,
+    p.add_argument("--cpu-sample-rows", type=int, default=8192,
                    help="rows per linear of one layer in the oracle's sample")
     return p.parse_args()
 
@@ -224,18 +224,18 @@ def run_reference(args, rank, world):
         return
     import workloads as wl
     for _ in range(args.warmup):
-        oracle_sample_time(args, wl, max(8, args.cpu_sample_rows // 8), args.seed)
+        oracle_sample_time(args, wl, max(8, args.cpu_sample_rows // 64), args.seed)
     times = []
     weights = threads = 0
     for _ in range(args.steps):
-        dt, weights, threads = oracle_sample_time(args, wl, max(8, args.cpu_sample_rows // 8), args.seed)
+        dt, weights, threads = oracle_sample_time(args, wl, max(8, args.cpu_sample_rows // 64), args.seed)
         times.append(dt)
     sec = sum(times) / len(times)
     value = cpu_value(args, wl, sec, weights)
     step_ms = args.tokens / value * 1e3
     sample = ("oracle fp64 linear on layer 0's seven linears, %d output rows each, all %d tokens, "
               "14 variants; step time extrapolated by weight count to %d layers"
-              % (max(8, args.cpu_sample_rows // 8), args.tokens, args.layers))
+              % (max(8, args.cpu_sample_rows // 64), args.tokens, args.layers))
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -305,11 +305,13 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     torch.cuda.synchronize()
     t0, t1 = new_event(), new_event()
+    torch.cuda.profiler.start()       # bounds an ncu launch list to the timed region
     t0.record(stream)
     for s_i in range(args.steps):
         step(ev[s_i])
     t1.record(stream)
     torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
     barrier()
     clocks = sampler.stop() if sampler else None
     ms_per_step = t0.elapsed_time(t1) / args.steps
