@@ -54,6 +54,9 @@ def parse_args():
     p.add_argument("--variants", type=int, default=14)
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-rows", action="store_true", help="skip the compress/prefill/single rows")
+    p.add_argument("--only", choices=["compress", "prefill", "single"], default=None,
+                   help="run just one row (for profiling); prints only that row")
+    p.add_argument("--compress-variants", type=int, default=14)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample-rows", type=int, default=8192,
                    help="rows per linear of one layer in the oracle's sample")
@@ -404,13 +407,25 @@ def time_events(torch, fn, iters, stream):
     return a.elapsed_time(b) / iters
 
 
-def run_rows(args, torch, bd, wl, dev, pk):
+def run_rows(args, torch, bd, wl, dev, pk, which=("compress", "prefill", "single")):
     """Compress, prefill and the single-linear decode on their own workloads."""
-    stream = torch.cuda.current_stream()
     rows = {}
-    # compress: 14 variants of one 28672 x 8192 bf16 matrix (inputs 6.6 GB)
     g = wl.generator(args.seed + 50, dev)
-    N, K, V = 28672, 8192, 14
+    if "compress" in which:
+        rows["compress"] = row_compress(args, torch, bd, wl, dev, pk, g)
+        torch.cuda.empty_cache()
+    if "prefill" in which:
+        rows["prefill"] = row_prefill(args, torch, bd, wl, dev, pk, g)
+        torch.cuda.empty_cache()
+    if "single" in which:
+        rows["single4096"] = row_single(args, torch, bd, wl, dev, pk, g)
+    return rows
+
+
+def row_compress(args, torch, bd, wl, dev, pk, g):
+    """14 variants of one 28672 x 8192 bf16 matrix (inputs 6.6 GB)."""
+    stream = torch.cuda.current_stream()
+    N, K, V = 28672, 8192, args.compress_variants
     wb = wl.base_weights(N, K, g, dev)
     wfs = [wl.finetuned_weights(wb, 1e-3, g) for _ in range(V)]
     alphas = torch.empty(V, dtype=torch.float32, device=dev)
@@ -423,16 +438,18 @@ def run_rows(args, torch, bd, wl, dev, pk):
     for _ in range(3):
         compress_all()
     ms = time_events(torch, compress_all, 5, stream)
-    cbytes = V * (2 * 2 * N * K + N * K // 8)
-    ach = cbytes / (ms / 1e3) / 1e9
-    rows["compress"] = {"workload": "14 variants of 28672x8192 bf16", "ms": ms,
-                        "roofline": {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
-                                     "unit": "GB/s", "frac": ach / pk["hbm_gbs"],
-                                     "traffic": profiled_traffic("compress_prefill14")}}
-    del wfs
-    torch.cuda.empty_cache()
+    per = 2 * 2 * N * K + N * K // 8
+    ach = V * per / (ms / 1e3) / 1e9
+    return {"workload": "%d variants of 28672x8192 bf16" % V, "ms": ms, "launches": V,
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": ach / pk["hbm_gbs"], "alg_bytes_per_launch": per,
+                         "traffic": profiled_traffic("compress_28672x8192")}}
 
-    # prefill: gate and up (28672 x 8192), 4 variants x 4096 tokens grouped
+
+def row_prefill(args, torch, bd, wl, dev, pk, g):
+    """gate and up (28672 x 8192), 4 variants x 4096 tokens grouped."""
+    stream = torch.cuda.current_stream()
+    N, K = 28672, 8192
     Vp, per = 4, 4096
     ids = wl.variant_ids_blocks([per] * Vp).to(dev)
     Mp = ids.numel()
@@ -446,6 +463,7 @@ def run_rows(args, torch, bd, wl, dev, pk):
     x = wl.activations(Mp, K, g, dev)
     y = torch.empty((Mp, N), dtype=torch.bfloat16, device=dev)
     wsp = bd.linear_workspace(Mp, N, K, Vp, dev)
+    bd.group(ids, Vp, wsp)
     path = pick_path(bd, "prefill_tc" if args.path == "auto" else args.path,
                      lambda p: bd.linear_grouped(x, mats[0][0], al, mats[0][2], Vp, y, wsp, path=p))
 
@@ -458,16 +476,15 @@ def run_rows(args, torch, bd, wl, dev, pk):
     ms = time_events(torch, prefill, 3, stream)
     flops = 2 * 2 * Mp * N * K
     tf = flops / (ms / 1e3) / 1e12
-    rows["prefill"] = {"workload": "gate+up 28672x8192, 4 variants x 4096 tokens", "ms": ms,
-                       "path": path,
-                       "roofline": {"bound": "tensor", "achieved": tf, "peak": pk["bf16_tflops"],
-                                    "unit": "TFLOP/s", "frac": tf / pk["bf16_tflops"],
-                                    "traffic": None}}
-    del mats, x, y
-    torch.cuda.empty_cache()
+    return {"workload": "gate+up 28672x8192, 4 variants x 4096 tokens", "ms": ms, "path": path,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": pk["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": tf / pk["bf16_tflops"], "traffic": None}}
 
-    # single 4096 x 4096 linear, 1 variant, M in {1, 8, 32, 64}; enough weight
-    # copies rotate that every call reads from HBM (> 2x L2)
+
+def row_single(args, torch, bd, wl, dev, pk, g):
+    """Single 4096 x 4096 linear, 1 variant, M in {1, 8, 32, 64}; 16 weight
+    copies rotate so that every call reads from HBM (> 2x L2)."""
+    stream = torch.cuda.current_stream()
     N = K = 4096
     copies = 16
     ws_list = []
@@ -493,8 +510,7 @@ def run_rows(args, torch, bd, wl, dev, pk):
         byt = linear_bytes(M, N, K, 1)
         ach = byt / (ms / 1e3) / 1e9
         single["M=%d" % M] = {"us": ms * 1e3, "achieved_gbs": ach, "frac": ach / pk["hbm_gbs"]}
-    rows["single4096"] = single
-    return rows
+    return single
 
 
 def pick_path(bd, preferred, call):
@@ -506,6 +522,17 @@ def pick_path(bd, preferred, call):
         if e.code != bd.BD_ERR_UNSUPPORTED:
             raise
         return "auto"
+
+
+def run_only(args):
+    import torch
+    import bit_delta_compressed_gb300 as bd
+    import workloads as wl
+    bd.get_lib()
+    dev = torch.device("cuda", 0)
+    pk, _ = peaks()
+    rows = run_rows(args, torch, bd, wl, dev, pk, which=(args.only,))
+    print(json.dumps({"rows": rows}), flush=True)
 
 
 def main():
@@ -520,6 +547,9 @@ def main():
         import torch
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl")
+    if args.only:
+        run_only(args)
+        return
     try:
         run_ours(args, rank, world, local_rank)
     finally:
