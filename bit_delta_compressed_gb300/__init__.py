@@ -43,6 +43,7 @@ SIGNATURES = {
     "bitdelta_compress_workspace": (_SZ, [_I64, _I64]),
     "bitdelta_compress": (_ST, [_P, _P, _ST, _I64, _I64, _P, _P, _P, _SZ, _P]),
     "bitdelta_compress_rows": (_ST, [_P, _P, _ST, _I64, _I64, _P, _P, _P]),
+    "bitdelta_compress_noalloc": (_ST, [_P, _P, _ST, _I64, _I64, _P, _P, _P]),
     "bitdelta_linear_workspace": (_SZ, [_I64, _I64, _I64, _I32]),
     "bitdelta_linear": (_ST, [_P, _P, _I64, _I64, _I64, _P, _P, _P, _I32, _P, _ST, _P, _SZ, _P]),
     "bitdelta_linear_ex": (_ST, [_P, _P, _I64, _I64, _I64, _P, _P, _P, _I32, _P, _ST, _P, _SZ,

@@ -16,6 +16,8 @@
 // and the last block to finish (an atomic ticket) adds the partials in a fixed
 // order and writes alpha = f32(sum / n).  Grid size depends only on the shape
 // and the device, so the result is bit-reproducible on a given device.
+#include <mutex>
+
 #include "bd_internal.cuh"
 
 namespace bd {
@@ -262,5 +264,83 @@ extern "C" bd_status bitdelta_compress_rows(const void* w_ft, const void* w_base
         compress_rows_kernel<true><<<static_cast<unsigned>(N), kThreads, 0, s>>>(ft, bs, bits, K, alpha_out);
     else
         compress_rows_kernel<false><<<static_cast<unsigned>(N), kThreads, 0, s>>>(ft, bs, bits, K, alpha_out);
+    return launch_status();
+}
+
+// ---------------------------------------------------------------------------
+// bitdelta_compress_noalloc: the same compression kernel, for callers that
+// cannot allocate device memory.  Some hosts of this library run where
+// cudaMalloc is off limits: inside an inference engine whose memory pool owns
+// every byte of the device, in a plugin that must not grow the process's
+// footprint, or in code on a path where an allocation would synchronise the
+// device.  They still pass inputs and outputs; the kernel's only scratch (one
+// fp64 partial per block plus the finishing ticket) lives in the static
+// device array below instead of a caller workspace.
+//
+// The array is shared by every call on a device and keeps the previous call's
+// contents; the ticket is cleared before each launch.  Two calls that overlap
+// on the GPU (different streams, no ordering between them) race on it and
+// give wrong results.  Every GPU that loads the library holds the array until
+// the process exits.
+// ---------------------------------------------------------------------------
+namespace bd {
+namespace {
+
+constexpr int kNoAllocMaxBlocks = 2048;
+constexpr size_t kNoAllocScratchBytes = kHeaderBytes + sizeof(double) * kNoAllocMaxBlocks;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of the static scratch on the current device.  In host code
+// the array's name stands for a host-side shadow, not device memory, so the
+// address is looked up once per device (with that device current) and cached.
+bd_status noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return BD_ERR_CUDA;
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return BD_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+            return BD_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return BD_OK;
+}
+
+}  // namespace
+}  // namespace bd
+
+extern "C" bd_status bitdelta_compress_noalloc(const void* w_ft, const void* w_base,
+                                               bd_dtype in_dtype, int64_t N, int64_t K,
+                                               float* alpha_out, uint32_t* bits_out,
+                                               void* stream) {
+    bd_status st = check_compress_args(w_ft, w_base, in_dtype, N, K, alpha_out, bits_out);
+    if (st != BD_OK) return st;
+    const bool f32 = (in_dtype == BD_F32);
+    const int64_t n_chunks = N * K / 8;
+    const int grid = compress_grid(n_chunks, f32);
+    if (grid > kNoAllocMaxBlocks) return BD_ERR_WORKSPACE;   // more partials than the array holds
+    void* scratch = nullptr;
+    st = noalloc_scratch(&scratch);
+    if (st != BD_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned* hdr = static_cast<unsigned*>(scratch);
+    if (cudaMemsetAsync(hdr + 1, 0, sizeof(unsigned), s) != cudaSuccess) return BD_ERR_CUDA;
+    CompressArgs a;
+    a.ft = static_cast<const uint4*>(w_ft);
+    a.base = static_cast<const uint4*>(w_base);
+    a.bits = reinterpret_cast<uint8_t*>(bits_out);
+    a.n_chunks = n_chunks;
+    a.partials = reinterpret_cast<double*>(static_cast<char*>(scratch) + kHeaderBytes);
+    a.ticket = hdr + 1;
+    a.alpha_out = alpha_out;
+    a.n_elems = static_cast<double>(N) * static_cast<double>(K);
+    if (f32) compress_kernel<true><<<grid, kThreads, 0, s>>>(a);
+    else compress_kernel<false><<<grid, kThreads, 0, s>>>(a);
     return launch_status();
 }

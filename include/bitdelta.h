@@ -108,6 +108,27 @@ bd_status bitdelta_compress_rows(const void *w_ft, const void *w_base, bd_dtype 
                                  int64_t N, int64_t K, float *alpha_out, uint32_t *bits_out,
                                  void *stream);
 
+/* bitdelta_compress for callers that cannot allocate device memory (an
+ * engine whose pool owns all device memory, a plugin that must not grow the
+ * footprint, a path where an allocation would synchronise the device).  The
+ * page has no counterpart: this is an interface convenience, not part of the
+ * method.  Arguments and results are those of bitdelta_compress minus the
+ * workspace; the scratch (one fp64 partial per block, at most 2048 blocks,
+ * 16.6 KB) is a static device array inside the library that every GPU
+ * loading the library keeps until the process exits.
+ *   - The first call on a device looks up that array's device address (with
+ *     the device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - All calls share the array and it keeps the last call's contents; the
+ *     finishing ticket is cleared on the stream before every launch.  Calls
+ *     that overlap on the GPU race on the array: order them on one stream.
+ *   - A matrix whose launch would need more than 2048 blocks is rejected with
+ *     BD_ERR_WORKSPACE before anything is enqueued.
+ * Calls no allocating routine. */
+bd_status bitdelta_compress_noalloc(const void *w_ft, const void *w_base, bd_dtype in_dtype,
+                                    int64_t N, int64_t K, float *alpha_out,
+                                    uint32_t *bits_out, void *stream);
+
 /* ------------------------------------------------------------------ */
 /* Multi-variant fused linear ("Serving architecture": W_eff =         */
 /* W_base + alpha_v * sign(delta_v), reconstructed on the fly and fused */
