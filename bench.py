@@ -73,22 +73,32 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def csrc_digest() -> str:
+KERNEL_SOURCES = {
+    "compress_28672x8192": ["bd_compress.cu", "bd_internal.cuh"],
+    "linear_stack70b": ["bd_linear.cu", "bd_paths.cuh", "bd_internal.cuh", "bd_decode_tc.cu",
+                        "bd_prefill_tc.cu", "bd_tc_common.cuh", "bd_sm100.cuh"],
+}
+
+
+def sources_digest(names) -> str:
+    """sha256 (16 hex) over the named kernel sources that exist."""
     h = hashlib.sha256()
-    for p in sorted((ROOT / "bit_delta_compressed_gb300" / "csrc").glob("*")):
-        h.update(p.name.encode())
-        h.update(p.read_bytes())
+    for n in names:
+        p = ROOT / "bit_delta_compressed_gb300" / "csrc" / n
+        if p.exists():
+            h.update(n.encode())
+            h.update(p.read_bytes())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(kernel_key: str):
-    """DRAM bytes per launch recorded from an ncu capture of the current
-    kernel sources (profiles/*.md lines 'traffic <key> <bytes> csrc <digest>'),
-    or None when absent or taken on older sources."""
-    digest = csrc_digest()
+    """DRAM bytes per launch from an ncu capture of the kernel's current
+    sources: a line 'traffic <key> <bytes> sources <digest>' in profiles/*.md.
+    None when absent or when the sources changed since the capture."""
+    digest = sources_digest(KERNEL_SOURCES.get(kernel_key, []))
     for f in sorted((ROOT / "profiles").glob("*.md")):
         for line in f.read_text().splitlines():
-            m = re.match(r"\s*traffic\s+(\S+)\s+([0-9.eE+]+)\s+csrc\s+(\w+)", line)
+            m = re.match(r"\s*traffic\s+(\S+)\s+([0-9.eE+]+)\s+sources\s+(\w+)", line)
             if m and m.group(1) == kernel_key and m.group(3) == digest:
                 return float(m.group(2))
     return None
@@ -559,4 +569,7 @@ def main():
 
 
 if __name__ == "__main__":
-    main()
+    if len(sys.argv) > 1 and sys.argv[1] == "--digest":
+        print(sources_digest(KERNEL_SOURCES[sys.argv[2]]))
+    else:
+        main()
