@@ -49,21 +49,51 @@ inline bd_status launch_status() {
 
 // ---- linear workspace layout (shared by the dispatcher and kernels) ----
 
+// Segment plan of one grouped batch, written by the grouping kernel.
+// Grouped positions: [0, n_base) base-model tokens (id -1), then every
+// present variant's tokens in variant order, then invalid ids.  For the
+// tensor-core decode path each present variant d also gets a zero-padded
+// segment of pad16(cnt[d]) rows starting at row seg[d] of the sign operand,
+// and the variants are cut into passes (groups) whose padded rows fit
+// `group_budget`.
+constexpr int kMaxGroups = BITDELTA_MAX_VARIANTS;
+struct SegPlan {
+    int32_t M;
+    int32_t n_base;
+    int32_t n_invalid;
+    int32_t D;                                    // present variants
+    int32_t P;                                    // sum of pad16(cnt)
+    int32_t n_groups;
+    int32_t var[BITDELTA_MAX_VARIANTS];           // variant id of present index d
+    int32_t cnt[BITDELTA_MAX_VARIANTS];           // its token count
+    int32_t off[BITDELTA_MAX_VARIANTS];           // grouped position of its first token
+    int32_t seg[BITDELTA_MAX_VARIANTS];           // first padded row of its segment
+    int32_t group_first[kMaxGroups + 1];          // present-index range of each pass
+};
+
 struct GroupView {
     int32_t* counts;     // [V + 2]: bucket 0 = id -1 (base), 1..V = variants, V+1 = invalid
     int32_t* offsets;    // [V + 3]: exclusive prefix of counts
     int32_t* pos2tok;    // [M]: grouped position -> original token
     int32_t* pos_var;    // [M]: grouped position -> variant id (-1 base, -2 invalid)
+    SegPlan* plan;
 };
+
+__host__ __device__ inline int pad16(int v) { return (v + 15) & ~15; }
 
 struct LinearWorkspace {
     unsigned* status;
     GroupView g;
+    size_t group_end;    // bytes up to the end of the grouping area
     void* tc_scratch;    // tensor-core paths: staged activations
     size_t tc_bytes;
     size_t total;
 };
 
 LinearWorkspace linear_workspace_layout(void* base, int64_t M, int64_t N, int64_t K, int32_t V);
+
+// Padded sign rows one pass of the tensor-core decode kernel can hold in
+// tensor memory next to the base accumulator of pad16(M) columns.
+int decode_group_budget(int64_t M);
 
 }  // namespace bd

@@ -34,6 +34,8 @@ LinearWorkspace linear_workspace_layout(void* base, int64_t M, int64_t N, int64_
     w.g.offsets = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (V + 3)));
     w.g.pos2tok = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (m ? m : 1)));
     w.g.pos_var = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (m ? m : 1)));
+    w.g.plan = reinterpret_cast<SegPlan*>(take(sizeof(SegPlan)));
+    w.group_end = off;
     w.tc_bytes = tc_scratch_bytes(M, N, K, V);
     w.tc_scratch = w.tc_bytes ? take(w.tc_bytes) : nullptr;
     w.total = off;
@@ -54,7 +56,8 @@ __device__ __forceinline__ int bucket_of(int32_t id, int V) {
 }
 
 __global__ void __launch_bounds__(1024) group_kernel(const int32_t* __restrict__ ids, int M, int V,
-                                                     GroupView g, unsigned* status) {
+                                                     int group_budget, GroupView g,
+                                                     unsigned* status) {
     extern __shared__ int sm[];
     const int nb = V + 2;
     int* hist = sm;                    // [32][nb] per-warp counts of the current slice
@@ -80,6 +83,33 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t* __restrict__
             run += total[b];
         }
         g.offsets[nb] = run;
+        // segment plan: present variants, padded segments, passes
+        SegPlan* pl = g.plan;
+        pl->M = M;
+        pl->n_base = total[0];
+        pl->n_invalid = total[V + 1];
+        int d = 0, rows = 0, groups = 0, group_rows = 0;
+        pl->group_first[0] = 0;
+        for (int v = 0; v < V; ++v) {
+            const int c = total[v + 1];
+            if (c == 0) continue;
+            const int pr = pad16(c);
+            if (group_rows > 0 && group_rows + pr > group_budget) {
+                pl->group_first[++groups] = d;
+                group_rows = 0;
+            }
+            pl->var[d] = v;
+            pl->cnt[d] = c;
+            pl->off[d] = start[v + 1];
+            pl->seg[d] = rows;
+            rows += pr;
+            group_rows += pr;
+            ++d;
+        }
+        pl->D = d;
+        pl->P = rows;
+        pl->n_groups = groups + 1;
+        pl->group_first[groups + 1] = d;
     }
     __syncthreads();
     for (int s0 = 0; s0 < M; s0 += blockDim.x) {
@@ -193,7 +223,8 @@ bd_status launch_group(const int32_t* ids, int64_t M, int32_t V, const LinearWor
     if (threads > 1024) threads = 1024;
     if (threads < 32) threads = 32;
     const size_t smem = sizeof(int) * (32 * (V + 2) + 3 * (V + 2));
-    group_kernel<<<1, threads, smem, s>>>(ids, static_cast<int>(M), V, w.g, w.status);
+    group_kernel<<<1, threads, smem, s>>>(ids, static_cast<int>(M), V, decode_group_budget(M), w.g,
+                                          w.status);
     return launch_status();
 }
 
@@ -287,10 +318,7 @@ extern "C" bd_status bitdelta_group(const int32_t* variant_ids, int64_t M, int32
     if (!workspace) return BD_ERR_WORKSPACE;
     if (!aligned(workspace, 16)) return BD_ERR_ALIGN;
     LinearWorkspace w = linear_workspace_layout(workspace, M, 1, 32, V);
-    const size_t group_end = static_cast<size_t>(
-        reinterpret_cast<char*>(w.g.pos_var) - static_cast<char*>(workspace)) +
-        round_up(sizeof(int32_t) * static_cast<size_t>(M), kAlign);
-    if (ws_bytes < group_end) return BD_ERR_WORKSPACE;
+    if (ws_bytes < w.group_end) return BD_ERR_WORKSPACE;
     return launch_group(variant_ids, M, V, w, static_cast<cudaStream_t>(stream));
 }
 

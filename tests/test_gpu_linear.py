@@ -149,7 +149,8 @@ def test_prefill_gate(bd, o, path):
 
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("M,N,K,V", [(1, 8, 32, 1), (37, 100, 96, 3), (5, 129, 64, 0),
-                                     (300, 72, 160, 5), (17, 1000, 512, 64)])
+                                     (300, 72, 160, 5), (17, 1000, 512, 64), (37, 200, 128, 3),
+                                     (208, 384, 192, 14), (2, 130, 640, 2), (64, 1024, 4096, 14)])
 def test_ragged_and_edges(bd, o, path, M, N, K, V):
     g = wl.generator(M * 131 + N * 7 + K + V, DEV)
     wb = wl.base_weights(N, K, g, DEV)
@@ -182,6 +183,26 @@ def test_invalid_variant_ids(bd, o, path):
     ref = o.linear(bf16_np(x)[good], ids_h[good], bf16_np(wb), f32_np(alphas),
                    [bits_np(b) for b in bits])
     assert_y_close(y[good], ref, "valid tokens")
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_many_small_variants_multi_pass(bd, o, path):
+    """128 tokens spread two per variant over 64 variants plus base-model and
+    invalid tokens: the padded sign segments exceed one tensor-memory pass."""
+    g = wl.generator(60, DEV)
+    M, N, K, V = 128, 256, 256, 64
+    wb = wl.base_weights(N, K, g, DEV)
+    bits = random_bits(g, N, K, V)
+    alphas = torch.rand(V, generator=g, device=DEV) * 2e-3 + 1e-4
+    ids_h = np.repeat(np.arange(V, dtype=np.int32), 2)[:M]
+    ids_h[::9] = -1
+    rng = np.random.default_rng(61)
+    rng.shuffle(ids_h)
+    x = wl.activations(M, K, g, DEV)
+    ids = torch.from_numpy(ids_h).to(DEV)
+    y = run(bd, path, x, ids, wb, alphas, bits)
+    ref = oracle_y(o, x, ids, wb, alphas, bits)
+    assert_y_close(y, ref, "multi-pass")
 
 
 def test_empty_batch(bd):
