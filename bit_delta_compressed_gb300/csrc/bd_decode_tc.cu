@@ -7,23 +7,30 @@
 //
 // One CTA owns 128 output rows (the 128 lanes of tensor memory) and a slice
 // of K (split-K; the slices of a row tile are summed in a fixed order by the
-// CTA that finishes last).  Per 64-column K block:
-//   * a TMA producer warp loads the W_base tile (128 x 64 bf16), the batch's
-//     activations in grouped order (X_c, pad16(M) rows) and the activations
-//     of this pass's variants in 16-row zero-padded segments with the K order
-//     permuted inside every 32-column group (X_p);
-//   * eight expansion warps turn each present variant's sign bits into a
-//     +-1 bf16 tile straight in tensor memory: for a 32-bit word w of bits,
-//     register j = ((w << (15 - j)) & 0x80008000) ^ 0xBF80BF80 holds columns j
-//     and j + 16 (bit 1 -> +1.0, bit 0 -> -1.0), one shift and one LOP3 per
-//     pair; X_p carries the same column order so the products line up;
-//   * one thread issues the MMAs: D_base += W * X_c^T (A and B from shared
-//     memory) and, per variant, D_sign[seg] += S_v * X_p[seg]^T (A from
-//     tensor memory), both fp32 accumulators in tensor memory;
-//   * the epilogue computes y = D_base + alpha_v * D_sign with the f32 alpha.
-// Variants whose padded segments do not fit in tensor memory next to D_base
-// are handled in further passes over the same K slice; those passes reload
-// only X_p and bits, never W_base.
+// CTA that finishes last).  For every 64-column K block:
+//   * a TMA warp loads the W_base tile, the batch's activations in grouped
+//     order (X_c, bf16) and the sign operand's activations (X_p);
+//   * one issuer thread accumulates D_base += W * X_c^T (bf16, both operands
+//     in shared memory, fp32 accumulator in tensor memory);
+//   * eight expansion warps turn each present variant's sign bits into +-1
+//     in fp8 e4m3 straight in tensor memory: for a 32-bit word w of bits,
+//     register j = ((w << (7 - j)) & 0x80808080) ^ 0xB8B8B8B8 holds columns
+//     j, j+8, j+16, j+24 (bit 1 -> +1.0, bit 0 -> -1.0): one shift and one
+//     LOP3 per four weights;
+//   * eight more issuer threads (variants split between them; their MMAs
+//     overlap on the tensor pipe) accumulate D_sign[segment of v] +=
+//     S_v * X_p^T with kind::f8f6f4, A from tensor memory;
+//   * the epilogue writes y = D_base + alpha_v * 2^-sigma_t * D_sign.
+// X_p holds each token's activations scaled by a power of two 2^sigma_t
+// (largest magnitude in [128, 256)) and split exactly into two e4m3 terms,
+// hi = rn(x 2^sigma) and lo = rn(x 2^sigma - hi): every element within 2^9
+// of the token's largest magnitude is represented exactly, smaller ones to
+// 2^-17 of that maximum.  The columns inside each 32-column group are
+// permuted to match the register layout above.  Variants whose padded
+// segments do not fit next to D_base are handled in further passes over the
+// same K slice; those passes reload only X_p and bits, never W_base.
+#include <cuda_fp8.h>
+
 #include <mutex>
 
 #include "bd_sm100.cuh"
@@ -34,26 +41,31 @@ namespace bd {
 namespace {
 
 constexpr int kBN = 128;                  // output rows per CTA (TMEM lanes)
-constexpr int kBK = 64;                   // K per stage (one 128-byte swizzle atom)
+constexpr int kBK = 64;                   // K per stage
 constexpr int kStages = 2;
-constexpr int kSlots = 3;                 // TMEM staging slots for the +-1 A tiles
-constexpr int kSlotCols = 32;             // 64 bf16 per row = 32 TMEM columns
-constexpr int kBaseCol = kSlots * kSlotCols;
+constexpr int kIssuers = 8;               // sign-MMA issuer threads
+constexpr int kSlotCols = 8;              // one 32-column word of e4m3 per row
+constexpr int kStagingCols = kIssuers * 2 * kSlotCols;
+constexpr int kBaseCol = kStagingCols;
 constexpr int kTmemCols = 512;
-constexpr int kBitRing = 3;               // K blocks of bits in flight per thread
-constexpr int kMaxM = 208;               // pad16(M) must fit next to one variant's segment
-constexpr int kThreads = 320;             // warp 0 TMA, warp 1 MMA, warps 2..9 expand/epilogue
+constexpr int kBitStages = 2;             // bits stages, each two K blocks (16 bytes per row)
+constexpr int kMaxM = 176;                // pad16(M) must fit next to one variant's segment
 constexpr int kExpandWarps = 8;
+constexpr int kThreads = 32 * (2 + kIssuers + kExpandWarps);   // 576
+constexpr int kFirstIssuerWarp = 2;
+constexpr int kFirstExpandWarp = 2 + kIssuers;
 constexpr uint32_t kWaitLimit = 1u << 20;
 
 struct DecodeParams {
-    CUtensorMap tm_w;                     // W_base [N, K]
-    CUtensorMap tm_xc;                    // X_c [Mb, K]
-    CUtensorMap tm_xp;                    // X_p [P_bound, K]
-    const uint32_t* bits[BITDELTA_MAX_VARIANTS];
+    CUtensorMap tm_w;                     // W_base [N, K] bf16, box 128 rows
+    CUtensorMap tm_xc;                    // X_c [Mb, K] bf16, box Mb rows
+    CUtensorMap tm_xp;                    // X_p [P_bound, 2K] bytes (e4m3 hi|lo per 64-col block), box 16 rows
+    CUtensorMap tm_xp128;                 // the same, box 128 rows
+    CUtensorMap tm_bits[BITDELTA_MAX_VARIANTS];   // packed bits [N, K/32] u32, box 128 rows x 4 words
     const float* alphas;
     const SegPlan* plan;
     const int32_t* pos2tok;
+    const int32_t* sigma;                 // per token
     void* y;
     float* part;                          // [splits][M][N] when splits > 1
     unsigned* tickets;                    // [n_tiles]
@@ -62,11 +74,15 @@ struct DecodeParams {
     int M, N, K, Mb, budget, splits, y_bf16;
 };
 
+constexpr uint32_t kBitsTile = kBN * 16;  // one variant, 128 rows x 4 words
+
 struct SmemLayout {
     uint32_t w, xc, xp, bits, total;
     int dmax;
 };
 
+// dmax: most variants one pass can hold (each needs >= 16 padded rows and
+// >= 1 token)
 __host__ __device__ inline SmemLayout smem_layout(int Mb, int budget) {
     SmemLayout L;
     const uint32_t w_bytes = kBN * 128, xc_bytes = Mb * 128, xp_bytes = budget * 128;
@@ -74,19 +90,13 @@ __host__ __device__ inline SmemLayout smem_layout(int Mb, int budget) {
     L.xc = L.w + kStages * w_bytes;
     L.xp = L.xc + kStages * xc_bytes;
     L.bits = L.xp + kStages * xp_bytes;
-    L.dmax = budget / 16;
-    L.total = L.bits + kBitRing * L.dmax * 2 * kBN * 4;
+    L.dmax = min(budget / 16, Mb);
+    L.total = L.bits + kBitStages * L.dmax * kBitsTile;
     return L;
 }
 
-__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sm100::smem_u32(dst)), "l"(src)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+__device__ __forceinline__ float exp2i(int e) {      // exact 2^e, e in [-126, 127]
+    return __int_as_float((127 + e) << 23);
 }
 
 __device__ __forceinline__ void store_y(const DecodeParams& p, int split, int t, int n, float v) {
@@ -99,11 +109,29 @@ __device__ __forceinline__ void store_y(const DecodeParams& p, int split, int t,
     }
 }
 
+// Pass g of the plan: present-variant range and its padded rows.
+struct PassInfo {
+    int d0, d1, row0, rows;
+};
+__device__ __forceinline__ PassInfo pass_info(const SegPlan& pl, int g) {
+    PassInfo q;
+    q.d0 = pl.group_first[g];
+    q.d1 = pl.group_first[g + 1];
+    q.row0 = (q.d1 > q.d0) ? pl.seg[q.d0] : 0;
+    q.rows = (q.d1 > q.d0) ? pl.seg[q.d1 - 1] + pad16(pl.cnt[q.d1 - 1]) - q.row0 : 0;
+    return q;
+}
+
+// Variants of a pass handled by issuer i: local indices i, i + 8, ...
+__device__ __forceinline__ int issuer_count(int nd, int i) { return nd > i ? (nd - i + kIssuers - 1) / kIssuers : 0; }
+
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_constant__ DecodeParams p) {
     using namespace sm100;
     extern __shared__ uint8_t dsmem[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t bar_full[kStages], bar_empty[kStages], tm_full[kSlots], tm_empty[kSlots];
+    __shared__ uint64_t bar_full[kStages], bar_empty[kStages];
+    __shared__ uint64_t bits_full[kBitStages], bits_empty[kBitStages];
+    __shared__ uint64_t tm_full[kIssuers][2], tm_empty[kIssuers][2];
     __shared__ uint64_t acc_full, acc_empty;
     __shared__ uint32_t tmem_base;
     __shared__ SegPlan pl;
@@ -125,9 +153,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         for (int i = threadIdx.x; i < static_cast<int>(sizeof(SegPlan) / 4); i += blockDim.x) dst[i] = src[i];
     }
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) { mbar_init(&bar_full[s], 1); mbar_init(&bar_empty[s], 1); }
-        for (int j = 0; j < kSlots; ++j) { mbar_init(&tm_full[j], kExpandWarps); mbar_init(&tm_empty[j], 1); }
-        mbar_init(&acc_full, 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&bar_full[s], 1);
+            mbar_init(&bar_empty[s], 1 + kIssuers);       // every issuer releases every stage
+        }
+        for (int b = 0; b < kBitStages; ++b) {
+            mbar_init(&bits_full[b], 1);
+            mbar_init(&bits_empty[b], kExpandWarps);
+        }
+        for (int i = 0; i < kIssuers; ++i)
+            for (int h = 0; h < 2; ++h) {
+                mbar_init(&tm_full[i][h], 4);              // four lane-quarter warps per word
+                mbar_init(&tm_empty[i][h], 1);
+            }
+        mbar_init(&acc_full, 1 + kIssuers);
         mbar_init(&acc_empty, kExpandWarps);
         fence_mbar_init();
     }
@@ -144,65 +183,94 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             prefetch_tensormap(&p.tm_w);
             prefetch_tensormap(&p.tm_xc);
             prefetch_tensormap(&p.tm_xp);
-            uint32_t it = 0;
+            prefetch_tensormap(&p.tm_xp128);
+            uint32_t it = 0, bt = 0;
             bool ok = true;
             for (int g = 0; g < n_groups && ok; ++g) {
-                const int d0 = pl.group_first[g], d1 = pl.group_first[g + 1];
-                const int row0 = (d1 > d0) ? pl.seg[d0] : 0;
-                const int rows = (d1 > d0) ? pl.seg[d1 - 1] + pad16(pl.cnt[d1 - 1]) - row0 : 0;
-                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                const PassInfo q = pass_info(pl, g);
+                for (int kb = kb0; kb < kb1 && ok; ++kb, ++it) {
+                    if (kb == kb0 || (kb & 1) == 0) {
+                        // bits of every variant of the pass for the K-block pair kb & ~1
+                        const int b = bt % kBitStages;
+                        if (!(ok = mbar_wait(&bits_empty[b], ((bt / kBitStages) & 1) ^ 1, kWaitLimit, p.status, 8, p.diag))) break;
+                        mbar_expect_tx(&bits_full[b], (q.d1 - q.d0) * kBitsTile);
+                        uint8_t* sb = base + L.bits + b * (L.dmax * kBitsTile);
+                        for (int d = q.d0; d < q.d1; ++d)
+                            tma_load_2d(sb + (d - q.d0) * kBitsTile, &p.tm_bits[pl.var[d]], &bits_full[b],
+                                        2 * (kb & ~1), n0);
+                        ++bt;
+                    }
                     const int s = it % kStages;
                     if (!(ok = mbar_wait(&bar_empty[s], ((it / kStages) & 1) ^ 1, kWaitLimit, p.status, 1, p.diag))) break;
-                    const uint32_t bytes = rows * 128 + (g == 0 ? kBN * 128 + Mb * 128 : 0);
+                    const uint32_t bytes = q.rows * 128 + (g == 0 ? kBN * 128 + Mb * 128 : 0);
                     mbar_expect_tx(&bar_full[s], bytes);
-                    const int kc = kb * kBK;
                     uint8_t* sw = base + L.w + s * (kBN * 128);
                     uint8_t* sxc = base + L.xc + s * (Mb * 128);
                     uint8_t* sxp = base + L.xp + s * (p.budget * 128);
                     if (g == 0) {
-                        tma_load_2d(sw, &p.tm_w, &bar_full[s], kc, n0);
-                        for (int r = 0; r < Mb; r += 16) tma_load_2d(sxc + r * 128, &p.tm_xc, &bar_full[s], kc, r);
+                        tma_load_2d(sw, &p.tm_w, &bar_full[s], kb * kBK, n0);
+                        tma_load_2d(sxc, &p.tm_xc, &bar_full[s], kb * kBK, 0);
                     }
-                    for (int r = 0; r < rows; r += 16) tma_load_2d(sxp + r * 128, &p.tm_xp, &bar_full[s], kc, row0 + r);
+                    int r = 0;
+                    for (; r + 128 <= q.rows; r += 128)
+                        tma_load_2d(sxp + r * 128, &p.tm_xp128, &bar_full[s], kb * 128, q.row0 + r);
+                    for (; r < q.rows; r += 16)
+                        tma_load_2d(sxp + r * 128, &p.tm_xp, &bar_full[s], kb * 128, q.row0 + r);
                 }
             }
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
+        // ---------------- base-product issuer ----------------
         if (lane == 0) {
-            uint32_t it = 0, c = 0;
+            uint32_t it = 0;
             bool ok = true;
-            const uint32_t idesc_base = idesc_bf16(128, Mb);
+            const uint32_t idesc = idesc_bf16(128, Mb);
             for (int g = 0; g < n_groups && ok; ++g) {
-                const int d0 = pl.group_first[g], d1 = pl.group_first[g + 1];
-                const int row0 = (d1 > d0) ? pl.seg[d0] : 0;
-                if (g > 0 && !(ok = mbar_wait(&acc_empty, (g - 1) & 1, kWaitLimit, p.status, 2, p.diag))) break;
                 for (int i = 0; i < nkb && ok; ++i, ++it) {
                     const int s = it % kStages;
-                    if (!(ok = mbar_wait(&bar_full[s], (it / kStages) & 1, kWaitLimit, p.status, 3, p.diag))) break;
-                    tc_fence_after();
-                    const uint32_t sw = smem_u32(base + L.w + s * (kBN * 128));
-                    const uint32_t sxc = smem_u32(base + L.xc + s * (Mb * 128));
-                    const uint32_t sxp = smem_u32(base + L.xp + s * (p.budget * 128));
+                    if (!(ok = mbar_wait(&bar_full[s], (it / kStages) & 1, kWaitLimit, p.status, 2, p.diag))) break;
                     if (g == 0) {
-#pragma unroll
-                        for (int k16 = 0; k16 < 4; ++k16)
-                            mma_ss(tmem + kBaseCol, desc_sw128(sw + 32 * k16), desc_sw128(sxc + 32 * k16),
-                                   idesc_base, (i > 0 || k16 > 0) ? 1u : 0u);
-                    }
-                    for (int d = d0; d < d1 && ok; ++d, ++c) {
-                        const int j = c % kSlots;
-                        if (!(ok = mbar_wait(&tm_full[j], (c / kSlots) & 1, kWaitLimit, p.status, 4, p.diag))) break;
                         tc_fence_after();
-                        const int segr = pl.seg[d] - row0;
-                        const uint32_t dcol = kBaseCol + Mb + segr;
-                        const uint32_t idesc = idesc_bf16(128, pad16(pl.cnt[d]));
+                        const uint32_t sw = smem_u32(base + L.w + s * (kBN * 128));
+                        const uint32_t sxc = smem_u32(base + L.xc + s * (Mb * 128));
 #pragma unroll
                         for (int k16 = 0; k16 < 4; ++k16)
-                            mma_ts(tmem + dcol, tmem + j * kSlotCols + 8 * k16,
-                                   desc_sw128(sxp + segr * 128 + 32 * k16), idesc,
+                            mma_ss(tmem + kBaseCol, desc_sw128(sw + 32 * k16), desc_sw128(sxc + 32 * k16), idesc,
                                    (i > 0 || k16 > 0) ? 1u : 0u);
-                        mma_commit(&tm_empty[j]);
+                    }
+                    mma_commit(&bar_empty[s]);
+                }
+                if (ok) mma_commit(&acc_full);
+            }
+        }
+    } else if (warp < kFirstExpandWarp) {
+        // ---------------- sign-product issuers ----------------
+        if (lane == 0) {
+            const int me = warp - kFirstIssuerWarp;
+            uint32_t it = 0, u = 0;
+            bool ok = true;
+            for (int g = 0; g < n_groups && ok; ++g) {
+                const PassInfo q = pass_info(pl, g);
+                const int nd = q.d1 - q.d0;
+                if (g > 0 && !(ok = mbar_wait(&acc_empty, (g - 1) & 1, kWaitLimit, p.status, 3, p.diag))) break;
+                for (int i = 0; i < nkb && ok; ++i, ++it) {
+                    const int s = it % kStages;
+                    if (!(ok = mbar_wait(&bar_full[s], (it / kStages) & 1, kWaitLimit, p.status, 4, p.diag))) break;
+                    const uint32_t sxp = smem_u32(base + L.xp + s * (p.budget * 128));
+                    for (int dl = me; dl < nd && ok; dl += kIssuers) {
+                        const int d = q.d0 + dl;
+                        const int segr = pl.seg[d] - q.row0;
+                        const uint32_t dcol = kBaseCol + Mb + segr;
+                        const uint32_t idesc = idesc_e4m3(128, pad16(pl.cnt[d]));
+                        for (int h = 0; h < 2 && ok; ++h, ++u) {
+                            if (!(ok = mbar_wait(&tm_full[me][h], (u >> 1) & 1, kWaitLimit, p.status, 5, p.diag))) break;
+                            tc_fence_after();
+                            const uint32_t a = tmem + me * 2 * kSlotCols + h * kSlotCols;
+                            const uint32_t brow = sxp + segr * 128 + 32 * h;
+                            mma_ts_f8(tmem + dcol, a, desc_sw128(brow), idesc, (i > 0 || h > 0) ? 1u : 0u);
+                            mma_ts_f8(tmem + dcol, a, desc_sw128(brow + 64), idesc, 1u);
+                            mma_commit(&tm_empty[me][h]);
+                        }
                     }
                     mma_commit(&bar_empty[s]);
                 }
@@ -211,92 +279,87 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         }
     } else {
         // ---------------- expansion, then epilogue ----------------
-        const int e = warp - 2;
+        const int e = warp - kFirstExpandWarp;
         const int h = e / 4;                      // which 32-bit word of the 64-column block
-        const int q = warp % 4;                   // TMEM lane quarter this warp may access
-        const int r = 32 * q + lane;              // output row within the tile
+        const int q4 = warp % 4;                  // TMEM lane quarter this warp may access
+        const int r = 32 * q4 + lane;             // output row within the tile
         const int n = n0 + r;
         const bool row_ok = n < p.N;
-        const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
-        const int words_per_row = p.K / 32;
-        uint32_t* ring = reinterpret_cast<uint32_t*>(base + L.bits);
-        uint32_t c = 0;
+        const uint32_t lane_addr = static_cast<uint32_t>(32 * q4) << 16;
+        uint32_t ubase[kIssuers];                 // units given to each issuer in earlier passes
+#pragma unroll
+        for (int i = 0; i < kIssuers; ++i) ubase[i] = 0;
+        uint32_t bt = 0;
         bool ok = true;
         for (int g = 0; g < n_groups && ok; ++g) {
-            const int d0 = pl.group_first[g], d1 = pl.group_first[g + 1];
-            const int nd = d1 - d0;
-            const int row0 = (d1 > d0) ? pl.seg[d0] : 0;
-            auto issue = [&](int i) {
-                if (i < nkb && row_ok) {
-                    const int slot = i % kBitRing;
-                    for (int d = d0; d < d1; ++d) {
-                        const uint32_t* src = p.bits[pl.var[d]] + static_cast<int64_t>(n) * words_per_row +
-                                              2 * (kb0 + i) + h;
-                        cp_async4(ring + ((slot * L.dmax + (d - d0)) * 2 + h) * kBN + r, src);
-                    }
-                }
-                cp_async_commit();
-            };
-            for (int i = 0; i < kBitRing - 1; ++i) issue(i);
+            const PassInfo q = pass_info(pl, g);
+            const int nd = q.d1 - q.d0;
             for (int i = 0; i < nkb && ok; ++i) {
-                issue(i + kBitRing - 1);
-                cp_async_wait<kBitRing - 1>();
-                const int slot = i % kBitRing;
-                for (int d = d0; d < d1 && ok; ++d, ++c) {
-                    const uint32_t w = row_ok ? ring[((slot * L.dmax + (d - d0)) * 2 + h) * kBN + r] : 0u;
-                    const int j = c % kSlots;
-                    if (!(ok = mbar_wait(&tm_empty[j], ((c / kSlots) & 1) ^ 1, kWaitLimit, p.status, 5, p.diag))) break;
+                const int kb = kb0 + i;
+                const int b = bt % kBitStages;
+                if (i == 0 || (kb & 1) == 0) {
+                    if (!(ok = mbar_wait(&bits_full[b], (bt / kBitStages) & 1, kWaitLimit, p.status, 9, p.diag))) break;
+                }
+                const uint32_t* sb = reinterpret_cast<const uint32_t*>(base + L.bits + b * (L.dmax * kBitsTile)) +
+                                     r * 4 + 2 * (kb & 1) + h;
+                for (int dl = 0; dl < nd && ok; ++dl) {
+                    const int iss = dl % kIssuers;
+                    const uint32_t u = ubase[iss] + 2 * (i * issuer_count(nd, iss) + dl / kIssuers) + h;
+                    const uint32_t w = sb[dl * (kBitsTile / 4)];
+                    if (!(ok = mbar_wait(&tm_empty[iss][h], ((u >> 1) & 1) ^ 1, kWaitLimit, p.status, 6, p.diag))) break;
                     tc_fence_after();
-                    uint32_t v[16];
+                    uint32_t v[8];
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) v[jj] = ((w << (15 - jj)) & 0x80008000u) ^ 0xBF80BF80u;
-                    tmem_st16(tmem + lane_addr + j * kSlotCols + 16 * h, v);
+                    for (int j = 0; j < 8; ++j) v[j] = ((w << (7 - j)) & 0x80808080u) ^ 0xB8B8B8B8u;
+                    tmem_st8(tmem + lane_addr + iss * 2 * kSlotCols + h * kSlotCols, v);
                     tmem_st_wait();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&tm_full[j]);
+                    if (lane == 0) mbar_arrive(&tm_full[iss][h]);
+                }
+                if (i == nkb - 1 || (kb & 1) == 1) {        // done with this bits stage
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bits_empty[b]);
+                    ++bt;
                 }
             }
-            cp_async_wait<0>();
-            (void)nd;
+#pragma unroll
+            for (int i = 0; i < kIssuers; ++i) ubase[i] += 2 * nkb * issuer_count(nd, i);
             if (!ok) break;
             // ---- epilogue of pass g ----
-            if (!(ok = mbar_wait(&acc_full, g & 1, kWaitLimit, p.status, 6, p.diag))) break;
+            if (!(ok = mbar_wait(&acc_full, g & 1, kWaitLimit, p.status, 7, p.diag))) break;
             tc_fence_after();
             if (g == 0) {
-                // base-model tokens: y = D_base
-                for (int pos0 = 16 * h; pos0 < pl.n_base; pos0 += 32) {
-                    uint32_t b[16];
-                    tmem_ld16(tmem + lane_addr + kBaseCol + pos0, b);
+                for (int pos0 = 8 * h; pos0 < pl.n_base; pos0 += 16) {     // base-model tokens
+                    uint32_t b[8];
+                    tmem_ld8(tmem + lane_addr + kBaseCol + pos0, b);
                     tmem_ld_wait();
                     if (row_ok)
-                        for (int t = 0; t < 16 && pos0 + t < pl.n_base; ++t)
-                            store_y(p, split, p.pos2tok[pos0 + t], n, __uint_as_float(b[t]));
+#pragma unroll
+                        for (int t = 0; t < 8; ++t)
+                            if (pos0 + t < pl.n_base) store_y(p, split, p.pos2tok[pos0 + t], n, __uint_as_float(b[t]));
                 }
-                // invalid ids: zero rows
-                if (row_ok && h == 0)
+                if (row_ok && h == 0)                                          // invalid ids: zero rows
                     for (int pos = p.M - pl.n_invalid; pos < p.M; ++pos) store_y(p, split, p.pos2tok[pos], n, 0.f);
             }
-            for (int d = d0; d < d1; ++d) {
+            for (int d = q.d0; d < q.d1; ++d) {
                 const int cnt = pl.cnt[d], off = pl.off[d];
                 const float alpha = p.alphas[pl.var[d]];
-                const uint32_t scol = kBaseCol + Mb + (pl.seg[d] - row0);
-                for (int ci = h; 16 * ci < cnt; ci += 2) {
-                    const int pos0 = off + 16 * ci;
-                    const int a0 = pos0 & ~15;          // aligned base chunk(s) covering pos0..pos0+15
-                    uint32_t b0[16], b1[16], sg[16];
-                    tmem_ld16(tmem + lane_addr + kBaseCol + a0, b0);
-                    tmem_ld16(tmem + lane_addr + kBaseCol + a0 + 16, b1);
-                    tmem_ld16(tmem + lane_addr + scol + 16 * ci, sg);
+                const uint32_t scol = kBaseCol + Mb + (pl.seg[d] - q.row0);
+                for (int ci = h; 8 * ci < cnt; ci += 2) {
+                    const int pos0 = off + 8 * ci;
+                    uint32_t sg[8], bs[8];
+                    tmem_ld8(tmem + lane_addr + scol + 8 * ci, sg);
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) bs[t] = tmem_ld1(tmem + lane_addr + kBaseCol + pos0 + t);
                     tmem_ld_wait();
                     if (row_ok) {
-                        const int sh = pos0 - a0;
 #pragma unroll
-                        for (int t = 0; t < 16; ++t) {
-                            if (16 * ci + t >= cnt) break;
-                            const int k = sh + t;
-                            const float bv = __uint_as_float(k < 16 ? b0[k & 15] : b1[k & 15]);
-                            store_y(p, split, p.pos2tok[pos0 + t], n, fmaf(alpha, __uint_as_float(sg[t]), bv));
+                        for (int t = 0; t < 8; ++t) {
+                            if (8 * ci + t >= cnt) break;
+                            const int tok = p.pos2tok[pos0 + t];
+                            const float sc = alpha * exp2i(-p.sigma[tok]);
+                            store_y(p, split, tok, n, fmaf(sc, __uint_as_float(sg[t]), __uint_as_float(bs[t])));
                         }
                     }
                 }
@@ -320,11 +383,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             __threadfence();
             const int rows = min(kBN, p.N - n0);
             for (int idx = threadIdx.x; idx < p.M * rows; idx += blockDim.x) {
-                const int t = idx / rows, r = idx % rows;
+                const int t = idx / rows, rr = idx % rows;
                 float acc = 0.f;
                 for (int s = 0; s < p.splits; ++s)
-                    acc += __ldcg(p.part + (static_cast<int64_t>(s) * p.M + t) * p.N + n0 + r);
-                const int64_t o = static_cast<int64_t>(t) * p.N + n0 + r;
+                    acc += __ldcg(p.part + (static_cast<int64_t>(s) * p.M + t) * p.N + n0 + rr);
+                const int64_t o = static_cast<int64_t>(t) * p.N + n0 + rr;
                 if (p.y_bf16) static_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(acc);
                 else static_cast<float*>(p.y)[o] = acc;
             }
@@ -336,58 +399,103 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
 }
 
 // ---------------------------------------------------------------------------
-// Activation staging for one linear: X_c (grouped order, pad16(M) rows) and
-// X_p (each present variant's tokens in a 16-row zero-padded segment, K
-// permuted inside every 32-column group: output column 2j + h of the group
-// holds input column j + 16h).  One thread per 32-column group of one row.
+// Per-token scale: sigma_t with max_k |x[t,k]| * 2^sigma_t in [128, 256)
+// (0 for an all-zero row).  One block per token.
 // ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) token_scale_kernel(const uint16_t* __restrict__ x, int K,
+                                                          int32_t* __restrict__ sigma) {
+    const uint16_t* row = x + static_cast<int64_t>(blockIdx.x) * K;
+    uint32_t mx = 0;      // max |x| as a bf16 bit pattern (monotone for non-negative values)
+    for (int k = threadIdx.x; k < K; k += blockDim.x) mx = max(mx, static_cast<uint32_t>(row[k] & 0x7FFFu));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    __shared__ uint32_t red[8];
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) mx = max(mx, red[i]);
+        const int ex = static_cast<int>((mx >> 7) & 0xFF);      // biased exponent of the max
+        int sg = 0;
+        if (mx != 0 && ex != 0xFF) sg = 7 - (ex > 0 ? ex - 127 : -126);
+        sigma[blockIdx.x] = max(-120, min(120, sg));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Activation staging for one linear:
+//   X_c [Mb, K] bf16: grouped order, zero rows past the valid tokens;
+//   X_p [rows, 2K] bytes: each present variant's tokens in a 16-row
+//       zero-padded segment; per 64-column block 64 bytes of hi then 64 of lo
+//       (e4m3), byte 32w + 4j + b of a half holding column 32w + j + 8b.
+// One thread per (row, 64-column block).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t e4m3(float v) {
+    return static_cast<uint32_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+}
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
+    __half_raw hr = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(b), __NV_E4M3);
+    return __half2float(__half(hr));
+}
+
 __global__ void __launch_bounds__(256) stage_x_kernel(const uint4* __restrict__ x, int M, int K, int Mb,
                                                       const SegPlan* __restrict__ plan,
                                                       const int32_t* __restrict__ pos2tok,
+                                                      const int32_t* __restrict__ sigma,
                                                       uint4* __restrict__ xc, uint4* __restrict__ xp,
                                                       int p_rows) {
     const int rr = blockIdx.y;
-    const int grp = blockIdx.x * blockDim.x + threadIdx.x;      // 32-column group
-    if (grp >= K / 32) return;
-    const int64_t vec_per_row = K / 8;
+    const int blk = blockIdx.x * blockDim.x + threadIdx.x;      // 64-column block
+    if (blk >= K / 64) return;
+    const int64_t vec_per_row = K / 8;                            // 16-byte vectors per row
     int tok = -1;
-    bool perm = false;
-    uint4* dst;
     if (rr < Mb) {
         const int n_valid = plan->M - plan->n_invalid;
         tok = (rr < n_valid) ? pos2tok[rr] : -1;
-        dst = xc + static_cast<int64_t>(rr) * vec_per_row + 4 * grp;
-    } else {
-        const int q = rr - Mb;
-        if (q >= p_rows) return;
-        perm = true;
-        dst = xp + static_cast<int64_t>(q) * vec_per_row + 4 * grp;
-        if (q < plan->P) {
-            int d = 0;
-            while (d + 1 < plan->D && plan->seg[d + 1] <= q) ++d;
-            const int j = q - plan->seg[d];
-            if (j < plan->cnt[d]) tok = pos2tok[plan->off[d] + j];
-        }
-    }
-    uint4 in[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-    if (tok >= 0) {
-        const uint4* src = x + static_cast<int64_t>(tok) * vec_per_row + 4 * grp;
+        uint4* dst = xc + static_cast<int64_t>(rr) * vec_per_row + 8 * blk;
+        const uint4* src = x + static_cast<int64_t>(tok < 0 ? 0 : tok) * vec_per_row + 8 * blk;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) in[i] = __ldg(src + i);
-    }
-    if (!perm) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) dst[i] = in[i];
+        for (int i = 0; i < 8; ++i) dst[i] = tok >= 0 ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
         return;
     }
-    const uint32_t w[16] = {in[0].x, in[0].y, in[0].z, in[0].w, in[1].x, in[1].y, in[1].z, in[1].w,
-                            in[2].x, in[2].y, in[2].z, in[2].w, in[3].x, in[3].y, in[3].z, in[3].w};
-    uint32_t o[16];
+    const int q = rr - Mb;
+    if (q >= p_rows) return;
+    if (q < plan->P) {
+        int d = 0;
+        while (d + 1 < plan->D && plan->seg[d + 1] <= q) ++d;
+        const int j = q - plan->seg[d];
+        if (j < plan->cnt[d]) tok = pos2tok[plan->off[d] + j];
+    }
+    uint32_t hi[16], lo[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j)   // element j (low) and element j + 16 (high)
-        o[j] = __byte_perm(w[j >> 1], w[8 + (j >> 1)], (j & 1) ? 0x7632 : 0x5410);
+    for (int i = 0; i < 16; ++i) { hi[i] = 0; lo[i] = 0; }
+    if (tok >= 0) {
+        const uint4* src = x + static_cast<int64_t>(tok) * vec_per_row + 8 * blk;
+        uint32_t w[32];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+        for (int i = 0; i < 8; ++i) {
+            const uint4 v = __ldg(src + i);
+            w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+        }
+        const float sc = exp2i(sigma[tok]);
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {                     // source column c of the block
+            const uint32_t bits16 = (c & 1) ? (w[c >> 1] >> 16) : (w[c >> 1] & 0xFFFFu);
+            const float v = __uint_as_float(bits16 << 16) * sc;
+            const uint32_t h8 = e4m3(v);
+            const uint32_t l8 = e4m3(v - e4m3_to_f32(h8));
+            const int wd = c >> 5, cc = c & 31;             // word, column within it
+            const int jj = cc & 7, b = cc >> 3;             // register j, byte b
+            const int byte = 32 * wd + 4 * jj + b;
+            hi[byte >> 2] |= h8 << (8 * (byte & 3));
+            lo[byte >> 2] |= l8 << (8 * (byte & 3));
+        }
+    }
+    uint4* dst = xp + static_cast<int64_t>(q) * vec_per_row + 8 * blk;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        dst[i] = make_uint4(hi[4 * i], hi[4 * i + 1], hi[4 * i + 2], hi[4 * i + 3]);
+        dst[4 + i] = make_uint4(lo[4 * i], lo[4 * i + 1], lo[4 * i + 2], lo[4 * i + 3]);
+    }
 }
 
 int p_bound(int64_t M, int32_t V) {
@@ -409,7 +517,8 @@ int choose_splits(int64_t n_tiles, int kb_total, int sms) {
 
 struct DecodeScratch {
     uint16_t* xc;
-    uint16_t* xp;
+    uint8_t* xp;
+    int32_t* sigma;
     float* part;
     unsigned* tickets;
     size_t bytes;
@@ -426,7 +535,8 @@ DecodeScratch decode_scratch(void* base, int64_t M, int64_t N, int64_t K, int32_
     };
     const int Mb = pad16(static_cast<int>(M));
     d.xc = reinterpret_cast<uint16_t*>(take(static_cast<size_t>(Mb) * K * 2));
-    d.xp = reinterpret_cast<uint16_t*>(take(static_cast<size_t>(p_bound(M, V)) * K * 2));
+    d.xp = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(p_bound(M, V)) * K * 2));
+    d.sigma = reinterpret_cast<int32_t*>(take(static_cast<size_t>(M) * 4));
     const int64_t n_tiles = (N + kBN - 1) / kBN;
     d.part = splits > 1 ? reinterpret_cast<float*>(take(static_cast<size_t>(splits) * M * N * 4)) : nullptr;
     d.tickets = reinterpret_cast<unsigned*>(take(static_cast<size_t>(n_tiles) * 4));
@@ -465,8 +575,10 @@ bd_status launch_decode_tc(const LinearArgs& a, const LinearWorkspace& w, cudaSt
     if (sc.bytes > w.tc_bytes) return BD_ERR_WORKSPACE;
     const int prow = p_bound(a.M, a.V);
 
-    dim3 sg((K / 32 + 255) / 256, Mb + prow);
-    stage_x_kernel<<<sg, 256, 0, s>>>(static_cast<const uint4*>(a.x), M, K, Mb, w.g.plan, w.g.pos2tok,
+    token_scale_kernel<<<M, 256, 0, s>>>(static_cast<const uint16_t*>(a.x), K, sc.sigma);
+    if (launch_status() != BD_OK) return BD_ERR_CUDA;
+    dim3 sg((K / 64 + 255) / 256, Mb + prow);
+    stage_x_kernel<<<sg, 256, 0, s>>>(static_cast<const uint4*>(a.x), M, K, Mb, w.g.plan, w.g.pos2tok, sc.sigma,
                                       reinterpret_cast<uint4*>(sc.xc), reinterpret_cast<uint4*>(sc.xp), prow);
     if (launch_status() != BD_OK) return BD_ERR_CUDA;
     if (splits > 1 && cudaMemsetAsync(sc.tickets, 0, n_tiles * 4, s) != cudaSuccess) return BD_ERR_CUDA;
@@ -474,13 +586,16 @@ bd_status launch_decode_tc(const LinearArgs& a, const LinearWorkspace& w, cudaSt
     DecodeParams p;
     memset(&p, 0, sizeof p);
     if (!make_tmap_bf16_sw128(&p.tm_w, a.w_base, a.N, a.K, kBN) ||
-        !make_tmap_bf16_sw128(&p.tm_xc, sc.xc, Mb, a.K, 16) ||
-        !make_tmap_bf16_sw128(&p.tm_xp, sc.xp, prow, a.K, 16))
+        !make_tmap_bf16_sw128(&p.tm_xc, sc.xc, Mb, a.K, Mb) ||
+        !make_tmap_u8_sw128(&p.tm_xp, sc.xp, prow, 2 * a.K, 16) ||
+        !make_tmap_u8_sw128(&p.tm_xp128, sc.xp, prow, 2 * a.K, 128))
         return BD_ERR_CUDA;
-    for (int v = 0; v < a.V; ++v) p.bits[v] = reinterpret_cast<const uint32_t*>(a.bits.p[v]);
+    for (int v = 0; v < a.V; ++v)
+        if (!make_tmap_bits(&p.tm_bits[v], a.bits.p[v], a.N, a.K / 32, kBN)) return BD_ERR_CUDA;
     p.alphas = a.alphas;
     p.plan = w.g.plan;
     p.pos2tok = w.g.pos2tok;
+    p.sigma = sc.sigma;
     p.y = a.y;
     p.part = sc.part;
     p.tickets = sc.tickets;
@@ -507,22 +622,25 @@ namespace {
 std::mutex g_tc_mutex;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 int g_smem_set[64][4] = {};
+
+bool encoder() {
+    std::lock_guard<std::mutex> lock(g_tc_mutex);
+    if (!g_encode) {
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return false;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    return true;
+}
 }  // namespace
 
 bool make_tmap_bf16_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                           uint32_t box_rows) {
-    {
-        std::lock_guard<std::mutex> lock(g_tc_mutex);
-        if (!g_encode) {
-            cudaDriverEntryPointQueryResult q;
-            void* fn = nullptr;
-            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                                 &q) != cudaSuccess ||
-                q != cudaDriverEntryPointSuccess || !fn)
-                return false;
-            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-        }
-    }
+    if (!encoder()) return false;
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {cols * 2};
     cuuint32_t box[2] = {64, box_rows};
@@ -530,6 +648,29 @@ bool make_tmap_bf16_sw128(CUtensorMap* map, const void* base, uint64_t rows, uin
     return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
                     es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_tmap_u8_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols_bytes,
+                        uint32_t box_rows) {
+    if (!encoder()) return false;
+    cuuint64_t dims[2] = {cols_bytes, rows};
+    cuuint64_t strides[1] = {cols_bytes};
+    cuuint32_t box[2] = {128, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_tmap_bits(CUtensorMap* map, const void* base, uint64_t rows, uint64_t words, uint32_t box_rows) {
+    if (!encoder()) return false;
+    cuuint64_t dims[2] = {words, rows};
+    cuuint64_t strides[1] = {words * 4};
+    cuuint32_t box[2] = {4, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool set_smem_attr(const void* kernel, int bytes, int slot) {
