@@ -158,6 +158,22 @@ def gpu_uuid(torch, dev):
 
 # -- the workload ----------------------------------------------------------------
 
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The slowest rank's value (every rank passes its own)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(tokens_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Tokens per second over all ranks: every rank is an independent replica
+    processing its own batch in the same step time (weak scaling)."""
+    return tokens_per_rank * world / (ms_per_step / 1e3)
+
+
 def distinct_count(ids) -> int:
     return len(set(int(v) for v in ids))
 
@@ -327,12 +343,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.profiler.stop()
     barrier()
     clocks = sampler.stop() if sampler else None
-    ms_per_step = t0.elapsed_time(t1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms_per_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_per_step = float(t.item())
-    value = M * world / (ms_per_step / 1e3)
+    ms_per_step = max_over_ranks(t0.elapsed_time(t1) / args.steps, world, dev)
+    value = whole_job_rate(M, world, ms_per_step)
 
     # roofline of the dominant kernel: algorithmic bytes per launch over the
     # average launch duration inside the timed region

@@ -52,6 +52,7 @@ SIGNATURES = {
     "bitdelta_linear_grouped": (_ST, [_P, _I64, _I64, _I64, _P, _P, _P, _I32, _P, _ST, _P, _SZ,
                                       _P, _ST]),
     "bitdelta_device_status": (_ST, [_P, _P]),
+    "bitdelta_check_bounded_wait": (_ST, [_P, ctypes.c_uint32, ctypes.c_int, _P]),
     "bitdelta_status_string": (ctypes.c_char_p, [_ST]),
     "bitdelta_abi_version": (ctypes.c_int, []),
 }

@@ -47,3 +47,35 @@ extern "C" const char* bitdelta_status_string(bd_status s) {
 }
 
 extern "C" int bitdelta_abi_version(void) { return BITDELTA_ABI_VERSION; }
+
+// ---------------------------------------------------------------------------
+// Health check of the bounded waits the tensor-core kernels use: one thread
+// waits on an mbarrier for `poll_limit` polls.  With arrive != 0 the barrier
+// is completed first and the wait succeeds; otherwise nothing ever arrives,
+// the wait gives up, and BD_ERR_TIMEOUT is OR-ed into the workspace status
+// word (with where-code 99 in the diagnostic word) -- the device stays usable.
+// ---------------------------------------------------------------------------
+#include "bd_sm100.cuh"
+
+namespace bd {
+namespace {
+__global__ void bounded_wait_kernel(unsigned* status, uint32_t poll_limit, int arrive) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    sm100::mbar_init(&bar, 1);
+    sm100::fence_mbar_init();
+    if (arrive) sm100::mbar_arrive(&bar);
+    sm100::mbar_wait(&bar, 0, poll_limit, status, 99, status + 2);
+}
+}  // namespace
+}  // namespace bd
+
+extern "C" bd_status bitdelta_check_bounded_wait(void* workspace, uint32_t poll_limit, int arrive,
+                                                 void* stream) {
+    if (!workspace) return BD_ERR_NULL;
+    if (!bd::aligned(workspace, 16)) return BD_ERR_ALIGN;
+    if (poll_limit < 1 || poll_limit > (1u << 24)) return BD_ERR_SHAPE;
+    bd::bounded_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<unsigned*>(workspace), poll_limit, arrive);
+    return bd::launch_status();
+}

@@ -42,7 +42,8 @@ namespace {
 
 constexpr int kBN = 128;                  // output rows per CTA (TMEM lanes)
 constexpr int kBK = 64;                   // K per stage
-constexpr int kStages = 2;
+constexpr int kWStages = 4;               // W_base tiles in flight (HBM)
+constexpr int kXStages = 2;               // activation tiles in flight (L2)
 constexpr int kIssuers = 8;               // sign-MMA issuer threads
 constexpr int kSlotCols = 8;              // one 32-column word of e4m3 per row
 constexpr int kStagingCols = kIssuers * 2 * kSlotCols;
@@ -75,23 +76,23 @@ struct DecodeParams {
 };
 
 constexpr uint32_t kBitsTile = kBN * 16;  // one variant, 128 rows x 4 words
+constexpr uint32_t kWTile = kBN * 128;    // 128 rows x 64 bf16
 
+// Shared memory: W ring | activation ring (X_c rows then X_p rows per stage)
+// | bits ring (kMaxPassVariants tiles per stage).
 struct SmemLayout {
-    uint32_t w, xc, xp, bits, total;
-    int dmax;
+    uint32_t w, x, x_stage, xp_off, bits, bits_stage, total;
 };
 
-// dmax: most variants one pass can hold (each needs >= 16 padded rows and
-// >= 1 token)
 __host__ __device__ inline SmemLayout smem_layout(int Mb, int budget) {
     SmemLayout L;
-    const uint32_t w_bytes = kBN * 128, xc_bytes = Mb * 128, xp_bytes = budget * 128;
     L.w = 0;
-    L.xc = L.w + kStages * w_bytes;
-    L.xp = L.xc + kStages * xc_bytes;
-    L.bits = L.xp + kStages * xp_bytes;
-    L.dmax = min(budget / 16, Mb);
-    L.total = L.bits + kBitStages * L.dmax * kBitsTile;
+    L.x = kWStages * kWTile;
+    L.x_stage = (Mb + budget) * 128;
+    L.xp_off = Mb * 128;
+    L.bits = L.x + kXStages * L.x_stage;
+    L.bits_stage = kMaxPassVariants * kBitsTile;
+    L.total = L.bits + kBitStages * L.bits_stage;
     return L;
 }
 
@@ -129,7 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     using namespace sm100;
     extern __shared__ uint8_t dsmem[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t bar_full[kStages], bar_empty[kStages];
+    __shared__ uint64_t w_full[kWStages], w_empty[kWStages], x_full[kXStages], x_empty[kXStages];
     __shared__ uint64_t bits_full[kBitStages], bits_empty[kBitStages];
     __shared__ uint64_t tm_full[kIssuers][2], tm_empty[kIssuers][2];
     __shared__ uint64_t acc_full, acc_empty;
@@ -147,15 +148,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     const int kb1 = static_cast<int>(static_cast<int64_t>(split + 1) * kb_total / p.splits);
     const int nkb = kb1 - kb0;
 
-    {   // copy the segment plan into shared memory
-        const int* src = reinterpret_cast<const int*>(p.plan);
-        int* dst = reinterpret_cast<int*>(&pl);
-        for (int i = threadIdx.x; i < static_cast<int>(sizeof(SegPlan) / 4); i += blockDim.x) dst[i] = src[i];
-    }
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&bar_full[s], 1);
-            mbar_init(&bar_empty[s], 1 + kIssuers);       // every issuer releases every stage
+        for (int s = 0; s < kWStages; ++s) {
+            mbar_init(&w_full[s], 1);
+            mbar_init(&w_empty[s], 1);                     // the base issuer
+        }
+        for (int s = 0; s < kXStages; ++s) {
+            mbar_init(&x_full[s], 1);
+            mbar_init(&x_empty[s], 1 + kIssuers);         // every issuer releases every stage
         }
         for (int b = 0; b < kBitStages; ++b) {
             mbar_init(&bits_full[b], 1);
@@ -171,6 +171,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         fence_mbar_init();
     }
     if (warp == 1) tmem_alloc(&tmem_base, kTmemCols);
+    // everything above overlaps the staging kernel; from here on its outputs
+    // (activations, scales, tickets) are read
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    {   // copy the segment plan into shared memory
+        const int* src = reinterpret_cast<const int*>(p.plan);
+        int* dst = reinterpret_cast<int*>(&pl);
+        for (int i = threadIdx.x; i < static_cast<int>(sizeof(SegPlan) / 4); i += blockDim.x) dst[i] = src[i];
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -184,61 +192,67 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             prefetch_tensormap(&p.tm_xc);
             prefetch_tensormap(&p.tm_xp);
             prefetch_tensormap(&p.tm_xp128);
-            uint32_t it = 0, bt = 0;
+            uint32_t wt = 0, xt = 0, bt = 0;
             bool ok = true;
             for (int g = 0; g < n_groups && ok; ++g) {
                 const PassInfo q = pass_info(pl, g);
-                for (int kb = kb0; kb < kb1 && ok; ++kb, ++it) {
+                for (int kb = kb0; kb < kb1 && ok; ++kb) {
                     if (kb == kb0 || (kb & 1) == 0) {
                         // bits of every variant of the pass for the K-block pair kb & ~1
                         const int b = bt % kBitStages;
                         if (!(ok = mbar_wait(&bits_empty[b], ((bt / kBitStages) & 1) ^ 1, kWaitLimit, p.status, 8, p.diag))) break;
                         mbar_expect_tx(&bits_full[b], (q.d1 - q.d0) * kBitsTile);
-                        uint8_t* sb = base + L.bits + b * (L.dmax * kBitsTile);
+                        uint8_t* sb = base + L.bits + b * L.bits_stage;
                         for (int d = q.d0; d < q.d1; ++d)
                             tma_load_2d(sb + (d - q.d0) * kBitsTile, &p.tm_bits[pl.var[d]], &bits_full[b],
                                         2 * (kb & ~1), n0);
                         ++bt;
                     }
-                    const int s = it % kStages;
-                    if (!(ok = mbar_wait(&bar_empty[s], ((it / kStages) & 1) ^ 1, kWaitLimit, p.status, 1, p.diag))) break;
-                    const uint32_t bytes = q.rows * 128 + (g == 0 ? kBN * 128 + Mb * 128 : 0);
-                    mbar_expect_tx(&bar_full[s], bytes);
-                    uint8_t* sw = base + L.w + s * (kBN * 128);
-                    uint8_t* sxc = base + L.xc + s * (Mb * 128);
-                    uint8_t* sxp = base + L.xp + s * (p.budget * 128);
                     if (g == 0) {
-                        tma_load_2d(sw, &p.tm_w, &bar_full[s], kb * kBK, n0);
-                        tma_load_2d(sxc, &p.tm_xc, &bar_full[s], kb * kBK, 0);
+                        const int s = wt % kWStages;
+                        if (!(ok = mbar_wait(&w_empty[s], ((wt / kWStages) & 1) ^ 1, kWaitLimit, p.status, 1, p.diag))) break;
+                        mbar_expect_tx(&w_full[s], kWTile);
+                        tma_load_2d(base + L.w + s * kWTile, &p.tm_w, &w_full[s], kb * kBK, n0);
+                        ++wt;
                     }
+                    const int s = xt % kXStages;
+                    if (!(ok = mbar_wait(&x_empty[s], ((xt / kXStages) & 1) ^ 1, kWaitLimit, p.status, 10, p.diag))) break;
+                    mbar_expect_tx(&x_full[s], q.rows * 128 + (g == 0 ? Mb * 128 : 0));
+                    uint8_t* sx = base + L.x + s * L.x_stage;
+                    if (g == 0) tma_load_2d(sx, &p.tm_xc, &x_full[s], kb * kBK, 0);
+                    uint8_t* sxp = sx + L.xp_off;
                     int r = 0;
                     for (; r + 128 <= q.rows; r += 128)
-                        tma_load_2d(sxp + r * 128, &p.tm_xp128, &bar_full[s], kb * 128, q.row0 + r);
+                        tma_load_2d(sxp + r * 128, &p.tm_xp128, &x_full[s], kb * 128, q.row0 + r);
                     for (; r < q.rows; r += 16)
-                        tma_load_2d(sxp + r * 128, &p.tm_xp, &bar_full[s], kb * 128, q.row0 + r);
+                        tma_load_2d(sxp + r * 128, &p.tm_xp, &x_full[s], kb * 128, q.row0 + r);
+                    ++xt;
                 }
             }
         }
     } else if (warp == 1) {
         // ---------------- base-product issuer ----------------
         if (lane == 0) {
-            uint32_t it = 0;
+            uint32_t xt = 0;
             bool ok = true;
             const uint32_t idesc = idesc_bf16(128, Mb);
             for (int g = 0; g < n_groups && ok; ++g) {
-                for (int i = 0; i < nkb && ok; ++i, ++it) {
-                    const int s = it % kStages;
-                    if (!(ok = mbar_wait(&bar_full[s], (it / kStages) & 1, kWaitLimit, p.status, 2, p.diag))) break;
+                for (int i = 0; i < nkb && ok; ++i, ++xt) {
+                    const int s = xt % kXStages;
+                    if (!(ok = mbar_wait(&x_full[s], (xt / kXStages) & 1, kWaitLimit, p.status, 2, p.diag))) break;
                     if (g == 0) {
+                        const int ws = i % kWStages;
+                        if (!(ok = mbar_wait(&w_full[ws], (i / kWStages) & 1, kWaitLimit, p.status, 11, p.diag))) break;
                         tc_fence_after();
-                        const uint32_t sw = smem_u32(base + L.w + s * (kBN * 128));
-                        const uint32_t sxc = smem_u32(base + L.xc + s * (Mb * 128));
+                        const uint32_t sw = smem_u32(base + L.w + ws * kWTile);
+                        const uint32_t sxc = smem_u32(base + L.x + s * L.x_stage);
 #pragma unroll
                         for (int k16 = 0; k16 < 4; ++k16)
                             mma_ss(tmem + kBaseCol, desc_sw128(sw + 32 * k16), desc_sw128(sxc + 32 * k16), idesc,
                                    (i > 0 || k16 > 0) ? 1u : 0u);
+                        mma_commit(&w_empty[ws]);
                     }
-                    mma_commit(&bar_empty[s]);
+                    mma_commit(&x_empty[s]);
                 }
                 if (ok) mma_commit(&acc_full);
             }
@@ -254,9 +268,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                 const int nd = q.d1 - q.d0;
                 if (g > 0 && !(ok = mbar_wait(&acc_empty, (g - 1) & 1, kWaitLimit, p.status, 3, p.diag))) break;
                 for (int i = 0; i < nkb && ok; ++i, ++it) {
-                    const int s = it % kStages;
-                    if (!(ok = mbar_wait(&bar_full[s], (it / kStages) & 1, kWaitLimit, p.status, 4, p.diag))) break;
-                    const uint32_t sxp = smem_u32(base + L.xp + s * (p.budget * 128));
+                    const int s = it % kXStages;
+                    if (!(ok = mbar_wait(&x_full[s], (it / kXStages) & 1, kWaitLimit, p.status, 4, p.diag))) break;
+                    const uint32_t sxp = smem_u32(base + L.x + s * L.x_stage + L.xp_off);
                     for (int dl = me; dl < nd && ok; dl += kIssuers) {
                         const int d = q.d0 + dl;
                         const int segr = pl.seg[d] - q.row0;
@@ -272,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                             mma_commit(&tm_empty[me][h]);
                         }
                     }
-                    mma_commit(&bar_empty[s]);
+                    mma_commit(&x_empty[s]);
                 }
                 if (ok) mma_commit(&acc_full);
             }
@@ -300,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                 if (i == 0 || (kb & 1) == 0) {
                     if (!(ok = mbar_wait(&bits_full[b], (bt / kBitStages) & 1, kWaitLimit, p.status, 9, p.diag))) break;
                 }
-                const uint32_t* sb = reinterpret_cast<const uint32_t*>(base + L.bits + b * (L.dmax * kBitsTile)) +
+                const uint32_t* sb = reinterpret_cast<const uint32_t*>(base + L.bits + b * L.bits_stage) +
                                      r * 4 + 2 * (kb & 1) + h;
                 for (int dl = 0; dl < nd && ok; ++dl) {
                     const int iss = dl % kIssuers;
@@ -399,35 +413,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
 }
 
 // ---------------------------------------------------------------------------
-// Per-token scale: sigma_t with max_k |x[t,k]| * 2^sigma_t in [128, 256)
-// (0 for an all-zero row).  One block per token.
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) token_scale_kernel(const uint16_t* __restrict__ x, int K,
-                                                          int32_t* __restrict__ sigma) {
-    const uint16_t* row = x + static_cast<int64_t>(blockIdx.x) * K;
-    uint32_t mx = 0;      // max |x| as a bf16 bit pattern (monotone for non-negative values)
-    for (int k = threadIdx.x; k < K; k += blockDim.x) mx = max(mx, static_cast<uint32_t>(row[k] & 0x7FFFu));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    __shared__ uint32_t red[8];
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) mx = max(mx, red[i]);
-        const int ex = static_cast<int>((mx >> 7) & 0xFF);      // biased exponent of the max
-        int sg = 0;
-        if (mx != 0 && ex != 0xFF) sg = 7 - (ex > 0 ? ex - 127 : -126);
-        sigma[blockIdx.x] = max(-120, min(120, sg));
-    }
-}
-
-// ---------------------------------------------------------------------------
-// Activation staging for one linear:
+// Staging for one linear (one block per staged row):
 //   X_c [Mb, K] bf16: grouped order, zero rows past the valid tokens;
 //   X_p [rows, 2K] bytes: each present variant's tokens in a 16-row
 //       zero-padded segment; per 64-column block 64 bytes of hi then 64 of lo
-//       (e4m3), byte 32w + 4j + b of a half holding column 32w + j + 8b.
-// One thread per (row, 64-column block).
+//       (e4m3), byte 32w + 4j + b of a half holding column 32w + j + 8b, for
+//       x * 2^sigma_t with sigma_t chosen so that max_k |x[t,k]| 2^sigma_t
+//       lies in [128, 256) (0 for an all-zero row);
+//   sigma[t] for every token with a sign segment; the split-K tickets zeroed.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t e4m3(float v) {
     return static_cast<uint32_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
@@ -437,46 +430,75 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
     return __half2float(__half(hr));
 }
 
-__global__ void __launch_bounds__(256) stage_x_kernel(const uint4* __restrict__ x, int M, int K, int Mb,
-                                                      const SegPlan* __restrict__ plan,
-                                                      const int32_t* __restrict__ pos2tok,
-                                                      const int32_t* __restrict__ sigma,
-                                                      uint4* __restrict__ xc, uint4* __restrict__ xp,
-                                                      int p_rows) {
-    const int rr = blockIdx.y;
-    const int blk = blockIdx.x * blockDim.x + threadIdx.x;      // 64-column block
-    if (blk >= K / 64) return;
-    const int64_t vec_per_row = K / 8;                            // 16-byte vectors per row
-    int tok = -1;
+__global__ void __launch_bounds__(256) prep_kernel(const uint4* __restrict__ x, int K, int Mb,
+                                                   const SegPlan* __restrict__ plan,
+                                                   const int32_t* __restrict__ pos2tok, int32_t* __restrict__ sigma,
+                                                   uint4* __restrict__ xc, uint4* __restrict__ xp,
+                                                   unsigned* tickets, int n_tickets) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int rr = blockIdx.x;
+    const int64_t vec_per_row = K / 8;
+    if (rr == 0)
+        for (int i = threadIdx.x; i < n_tickets; i += blockDim.x) tickets[i] = 0u;
     if (rr < Mb) {
         const int n_valid = plan->M - plan->n_invalid;
-        tok = (rr < n_valid) ? pos2tok[rr] : -1;
-        uint4* dst = xc + static_cast<int64_t>(rr) * vec_per_row + 8 * blk;
-        const uint4* src = x + static_cast<int64_t>(tok < 0 ? 0 : tok) * vec_per_row + 8 * blk;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) dst[i] = tok >= 0 ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
+        const int tok = (rr < n_valid) ? pos2tok[rr] : -1;
+        uint4* dst = xc + static_cast<int64_t>(rr) * vec_per_row;
+        const uint4* src = x + static_cast<int64_t>(tok < 0 ? 0 : tok) * vec_per_row;
+        for (int64_t i = threadIdx.x; i < vec_per_row; i += blockDim.x)
+            dst[i] = tok >= 0 ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
         return;
     }
     const int q = rr - Mb;
-    if (q >= p_rows) return;
-    if (q < plan->P) {
+    if (q >= plan->P) return;                     // never loaded
+    int tok = -1;
+    {
         int d = 0;
         while (d + 1 < plan->D && plan->seg[d + 1] <= q) ++d;
         const int j = q - plan->seg[d];
         if (j < plan->cnt[d]) tok = pos2tok[plan->off[d] + j];
     }
-    uint32_t hi[16], lo[16];
+    uint4* dst = xp + static_cast<int64_t>(q) * vec_per_row;
+    if (tok < 0) {
+        for (int64_t i = threadIdx.x; i < vec_per_row; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
+        return;
+    }
+    const uint4* src = x + static_cast<int64_t>(tok) * vec_per_row;
+    // sigma_t from the largest |x| of the row (bf16 bit patterns order like magnitudes)
+    uint32_t mx = 0;
+    for (int64_t i = threadIdx.x; i < vec_per_row; i += blockDim.x) {
+        const uint4 v = __ldg(src + i);
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int i = 0; i < 16; ++i) { hi[i] = 0; lo[i] = 0; }
-    if (tok >= 0) {
-        const uint4* src = x + static_cast<int64_t>(tok) * vec_per_row + 8 * blk;
+        for (int k = 0; k < 4; ++k) mx = max(mx, max(w4[k] & 0x7FFFu, (w4[k] >> 16) & 0x7FFFu));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    __shared__ uint32_t red[8];
+    __shared__ int sig_s;
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 8; ++i) mx = max(mx, red[i]);
+        const int ex = static_cast<int>((mx >> 7) & 0xFF);      // biased exponent of the max
+        int sg = 0;
+        if (mx != 0 && ex != 0xFF) sg = 7 - (ex > 0 ? ex - 127 : -126);
+        sg = max(-120, min(120, sg));
+        sig_s = sg;
+        sigma[tok] = sg;
+    }
+    __syncthreads();
+    const float sc = exp2i(sig_s);
+    for (int blk = threadIdx.x; blk < K / 64; blk += blockDim.x) {
         uint32_t w[32];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const uint4 v = __ldg(src + i);
+            const uint4 v = __ldg(src + 8 * blk + i);
             w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
         }
-        const float sc = exp2i(sigma[tok]);
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) { hi[i] = 0; lo[i] = 0; }
 #pragma unroll
         for (int c = 0; c < 64; ++c) {                     // source column c of the block
             const uint32_t bits16 = (c & 1) ? (w[c >> 1] >> 16) : (w[c >> 1] & 0xFFFFu);
@@ -489,12 +511,12 @@ __global__ void __launch_bounds__(256) stage_x_kernel(const uint4* __restrict__ 
             hi[byte >> 2] |= h8 << (8 * (byte & 3));
             lo[byte >> 2] |= l8 << (8 * (byte & 3));
         }
-    }
-    uint4* dst = xp + static_cast<int64_t>(q) * vec_per_row + 8 * blk;
+        uint4* o = dst + 8 * blk;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        dst[i] = make_uint4(hi[4 * i], hi[4 * i + 1], hi[4 * i + 2], hi[4 * i + 3]);
-        dst[4 + i] = make_uint4(lo[4 * i], lo[4 * i + 1], lo[4 * i + 2], lo[4 * i + 3]);
+        for (int i = 0; i < 4; ++i) {
+            o[i] = make_uint4(hi[4 * i], hi[4 * i + 1], hi[4 * i + 2], hi[4 * i + 3]);
+            o[4 + i] = make_uint4(lo[4 * i], lo[4 * i + 1], lo[4 * i + 2], lo[4 * i + 3]);
+        }
     }
 }
 
@@ -575,13 +597,10 @@ bd_status launch_decode_tc(const LinearArgs& a, const LinearWorkspace& w, cudaSt
     if (sc.bytes > w.tc_bytes) return BD_ERR_WORKSPACE;
     const int prow = p_bound(a.M, a.V);
 
-    token_scale_kernel<<<M, 256, 0, s>>>(static_cast<const uint16_t*>(a.x), K, sc.sigma);
+    prep_kernel<<<Mb + prow, 256, 0, s>>>(static_cast<const uint4*>(a.x), K, Mb, w.g.plan, w.g.pos2tok, sc.sigma,
+                                          reinterpret_cast<uint4*>(sc.xc), reinterpret_cast<uint4*>(sc.xp),
+                                          sc.tickets, splits > 1 ? static_cast<int>(n_tiles) : 0);
     if (launch_status() != BD_OK) return BD_ERR_CUDA;
-    dim3 sg((K / 64 + 255) / 256, Mb + prow);
-    stage_x_kernel<<<sg, 256, 0, s>>>(static_cast<const uint4*>(a.x), M, K, Mb, w.g.plan, w.g.pos2tok, sc.sigma,
-                                      reinterpret_cast<uint4*>(sc.xc), reinterpret_cast<uint4*>(sc.xp), prow);
-    if (launch_status() != BD_OK) return BD_ERR_CUDA;
-    if (splits > 1 && cudaMemsetAsync(sc.tickets, 0, n_tiles * 4, s) != cudaSuccess) return BD_ERR_CUDA;
 
     DecodeParams p;
     memset(&p, 0, sizeof p);
@@ -611,7 +630,18 @@ bd_status launch_decode_tc(const LinearArgs& a, const LinearWorkspace& w, cudaSt
     const SmemLayout L = smem_layout(Mb, budget);
     const int smem = static_cast<int>(L.total) + 1024;
     if (!set_smem_attr(reinterpret_cast<const void*>(decode_tc_kernel), smem, 0)) return BD_ERR_CUDA;
-    decode_tc_kernel<<<static_cast<unsigned>(n_tiles * splits), kThreads, smem, s>>>(p);
+    // programmatic dependent launch: the kernel's set-up overlaps the staging
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(n_tiles * splits));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, decode_tc_kernel, p) != cudaSuccess) return BD_ERR_CUDA;
     return launch_status();
 }
 

@@ -93,7 +93,9 @@ struct LinearWorkspace {
 LinearWorkspace linear_workspace_layout(void* base, int64_t M, int64_t N, int64_t K, int32_t V);
 
 // Padded sign rows one pass of the tensor-core decode kernel can hold in
-// tensor memory next to the base accumulator of pad16(M) columns.
+// tensor memory next to the base accumulator of pad16(M) columns, and the
+// most variants one pass takes (bounded by its shared-memory bits ring).
 int decode_group_budget(int64_t M);
+constexpr int kMaxPassVariants = 12;
 
 }  // namespace bd

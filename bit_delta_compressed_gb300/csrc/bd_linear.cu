@@ -88,15 +88,16 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t* __restrict__
         pl->M = M;
         pl->n_base = total[0];
         pl->n_invalid = total[V + 1];
-        int d = 0, rows = 0, groups = 0, group_rows = 0;
+        int d = 0, rows = 0, groups = 0, group_rows = 0, group_vars = 0;
         pl->group_first[0] = 0;
         for (int v = 0; v < V; ++v) {
             const int c = total[v + 1];
             if (c == 0) continue;
             const int pr = pad16(c);
-            if (group_rows > 0 && group_rows + pr > group_budget) {
+            if (group_rows > 0 && (group_rows + pr > group_budget || group_vars == kMaxPassVariants)) {
                 pl->group_first[++groups] = d;
                 group_rows = 0;
+                group_vars = 0;
             }
             pl->var[d] = v;
             pl->cnt[d] = c;
@@ -104,6 +105,7 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t* __restrict__
             pl->seg[d] = rows;
             rows += pr;
             group_rows += pr;
+            ++group_vars;
             ++d;
         }
         pl->D = d;

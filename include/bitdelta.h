@@ -205,6 +205,17 @@ bd_status bitdelta_linear_ex(const void *x, const int32_t *variant_ids,
  * and return the lowest-numbered error it holds (BD_OK if none). */
 bd_status bitdelta_device_status(void *workspace, void *stream);
 
+/* Health check of the bounded waits inside the tensor-core kernels (the page
+ * has no counterpart; this is failure-detection plumbing).  One GPU thread
+ * waits on a barrier for `poll_limit` polls (1 .. 2^24).  With arrive != 0 the
+ * barrier completes first and nothing is reported; with arrive == 0 nothing
+ * arrives, the wait runs out and BD_ERR_TIMEOUT is OR-ed into the status word
+ * of `workspace` (any linear or compress workspace, >= 256 bytes), exactly as
+ * a stalled pipeline inside a kernel would report it.  Read it with
+ * bitdelta_device_status.  The device stays usable. */
+bd_status bitdelta_check_bounded_wait(void *workspace, uint32_t poll_limit, int arrive,
+                                      void *stream);
+
 /* Static English text for a status code. */
 const char *bitdelta_status_string(bd_status s);
 

@@ -105,3 +105,7 @@ def test_linear_argument_errors(bd):
 
 def test_status_needs_workspace(bd):
     assert bd.bitdelta_device_status(None, None) == bd.BD_ERR_NULL
+    assert bd.bitdelta_check_bounded_wait(None, 16, 0, None) == bd.BD_ERR_NULL
+    assert bd.bitdelta_check_bounded_wait(MISALIGNED, 16, 0, None) == bd.BD_ERR_ALIGN
+    assert bd.bitdelta_check_bounded_wait(FAKE, 0, 0, None) == bd.BD_ERR_SHAPE
+    assert bd.bitdelta_check_bounded_wait(FAKE, (1 << 24) + 1, 0, None) == bd.BD_ERR_SHAPE
