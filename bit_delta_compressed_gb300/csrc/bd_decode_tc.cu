@@ -137,6 +137,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     __shared__ uint32_t tmem_base;
     __shared__ SegPlan pl;
     __shared__ int last_cta;
+    __shared__ int32_t tok_s[kMaxM];            // grouped position -> token
+    __shared__ float scale_s[kMaxM];            // grouped position -> alpha_v * 2^-sigma_t
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Mb = p.Mb;
@@ -179,6 +181,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         int* dst = reinterpret_cast<int*>(&pl);
         for (int i = threadIdx.x; i < static_cast<int>(sizeof(SegPlan) / 4); i += blockDim.x) dst[i] = src[i];
     }
+    __syncthreads();
+    // per grouped position: token and the epilogue's scale of the sign product
+    for (int d = 0; d < pl.D; ++d) {
+        const float alpha = p.alphas[pl.var[d]];
+        for (int j = threadIdx.x; j < pl.cnt[d]; j += blockDim.x) {
+            const int pos = pl.off[d] + j;
+            const int tok = p.pos2tok[pos];
+            tok_s[pos] = tok;
+            scale_s[pos] = alpha * exp2i(-p.sigma[tok]);
+        }
+    }
+    for (int pos = threadIdx.x; pos < pl.n_base; pos += blockDim.x) tok_s[pos] = p.pos2tok[pos];
+    for (int pos = p.M - pl.n_invalid + threadIdx.x; pos < p.M; pos += blockDim.x) tok_s[pos] = p.pos2tok[pos];
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -351,14 +366,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                     if (row_ok)
 #pragma unroll
                         for (int t = 0; t < 8; ++t)
-                            if (pos0 + t < pl.n_base) store_y(p, split, p.pos2tok[pos0 + t], n, __uint_as_float(b[t]));
+                            if (pos0 + t < pl.n_base) store_y(p, split, tok_s[pos0 + t], n, __uint_as_float(b[t]));
                 }
                 if (row_ok && h == 0)                                          // invalid ids: zero rows
-                    for (int pos = p.M - pl.n_invalid; pos < p.M; ++pos) store_y(p, split, p.pos2tok[pos], n, 0.f);
+                    for (int pos = p.M - pl.n_invalid; pos < p.M; ++pos) store_y(p, split, tok_s[pos], n, 0.f);
             }
             for (int d = q.d0; d < q.d1; ++d) {
                 const int cnt = pl.cnt[d], off = pl.off[d];
-                const float alpha = p.alphas[pl.var[d]];
                 const uint32_t scol = kBaseCol + Mb + (pl.seg[d] - q.row0);
                 for (int ci = h; 8 * ci < cnt; ci += 2) {
                     const int pos0 = off + 8 * ci;
@@ -371,9 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
 #pragma unroll
                         for (int t = 0; t < 8; ++t) {
                             if (8 * ci + t >= cnt) break;
-                            const int tok = p.pos2tok[pos0 + t];
-                            const float sc = alpha * exp2i(-p.sigma[tok]);
-                            store_y(p, split, tok, n, fmaf(sc, __uint_as_float(sg[t]), __uint_as_float(bs[t])));
+                            store_y(p, split, tok_s[pos0 + t], n,
+                                    fmaf(scale_s[pos0 + t], __uint_as_float(sg[t]), __uint_as_float(bs[t])));
                         }
                     }
                 }
@@ -525,14 +538,19 @@ int p_bound(int64_t M, int32_t V) {
     return pad16(static_cast<int>(M + 15 * d));
 }
 
-int choose_splits(int64_t n_tiles, int kb_total, int sms) {
+// K slices per row tile: minimise waves x (per-CTA fixed cost + K blocks per
+// slice x time per K block), both in microseconds as measured on GB300 for a
+// 128-token batch (the fixed cost covers set-up, pipeline fill, epilogue and
+// the split-K reduction).
+int choose_splits(int64_t n_tiles, int kb_total, int sms, int variants) {
+    const double fixed_us = 6.0, kb_us = 0.3 + 0.07 * variants;
     int best = 1;
-    double best_eff = 0.0;
-    for (int s = 1; s <= 64 && kb_total / s >= 4; ++s) {
+    double best_t = 1e30;
+    for (int s = 1; s <= 64 && s <= kb_total; ++s) {
         const int64_t ctas = n_tiles * s;
         const int64_t waves = (ctas + sms - 1) / sms;
-        const double eff = static_cast<double>(ctas) / static_cast<double>(waves * sms);
-        if (eff > best_eff + 0.02) { best_eff = eff; best = s; }
+        const double t = static_cast<double>(waves) * (fixed_us + ((kb_total + s - 1) / s) * kb_us);
+        if (t < best_t * 0.98) { best_t = t; best = s; }
     }
     return best;
 }
@@ -582,7 +600,7 @@ bool decode_tc_supported(const LinearArgs& a) {
 size_t decode_tc_scratch_bytes(int64_t M, int64_t N, int64_t K, int32_t V) {
     if (M < 1 || M > kMaxM || K % kBK != 0) return 0;
     const int64_t n_tiles = (N + kBN - 1) / kBN;
-    const int splits = choose_splits(n_tiles, static_cast<int>(K / kBK), sm_count());
+    const int splits = choose_splits(n_tiles, static_cast<int>(K / kBK), sm_count(), V < M ? V : static_cast<int>(M));
     return decode_scratch(nullptr, M, N, K, V, splits).bytes;
 }
 
@@ -592,7 +610,7 @@ bd_status launch_decode_tc(const LinearArgs& a, const LinearWorkspace& w, cudaSt
     const int budget = decode_group_budget(M);
     const int64_t n_tiles = (a.N + kBN - 1) / kBN;
     const int kb_total = K / kBK;
-    const int splits = choose_splits(n_tiles, kb_total, sm_count());
+    const int splits = choose_splits(n_tiles, kb_total, sm_count(), a.V < M ? a.V : M);
     DecodeScratch sc = decode_scratch(w.tc_scratch, a.M, a.N, a.K, a.V, splits);
     if (sc.bytes > w.tc_bytes) return BD_ERR_WORKSPACE;
     const int prow = p_bound(a.M, a.V);

@@ -219,6 +219,107 @@ simt_linear_kernel(const uint4* __restrict__ x, const uint4* __restrict__ w_base
     }
 }
 
+// ---------------------------------------------------------------------------
+// Small-batch CUDA-core path (M <= 4): a GEMV per output row.  One warp per
+// row; each lane issues U 16-byte weight loads (plus the matching activation
+// vectors and bits bytes) before doing any arithmetic, so enough bytes are in
+// flight per SM to stream W_base at full HBM bandwidth.
+// ---------------------------------------------------------------------------
+template <int MT, int U>
+__global__ void __launch_bounds__(kSimtWarps * 32)
+gemv_kernel(const uint4* __restrict__ x, const uint4* __restrict__ w_base,
+            const float* __restrict__ alphas, BitsTable bt, int M, int64_t N, int64_t K,
+            GroupView g, void* y, int y_bf16) {
+    const int lane = threadIdx.x & 31;
+    const int64_t n = static_cast<int64_t>(blockIdx.x) * kSimtWarps + (threadIdx.x >> 5);
+    if (n >= N) return;
+    const int64_t kc = K / 8;
+    int tok[MT], var[MT];
+    const uint8_t* bp[MT];
+#pragma unroll
+    for (int j = 0; j < MT; ++j) {
+        tok[j] = (j < M) ? g.pos2tok[j] : -1;
+        var[j] = (j < M) ? g.pos_var[j] : -2;
+        if (var[j] == -2) tok[j] = -1;                      // invalid id: zero row
+        bp[j] = (var[j] >= 0) ? bt.p[var[j]] + n * kc : nullptr;
+    }
+    float accb[MT], accs[MT];
+#pragma unroll
+    for (int j = 0; j < MT; ++j) { accb[j] = 0.f; accs[j] = 0.f; }
+    const uint4* wrow = w_base + n * kc;
+    auto chunk = [&](const uint4& wv, const uint4 (&xv)[MT], const uint32_t (&bb)[MT]) {
+        const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+        float wf[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) { wf[2 * i] = bf16_lo(ww[i]); wf[2 * i + 1] = bf16_hi(ww[i]); }
+#pragma unroll
+        for (int j = 0; j < MT; ++j) {
+            if (tok[j] < 0) continue;
+            const uint32_t xw[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+            float xf[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) { xf[2 * i] = bf16_lo(xw[i]); xf[2 * i + 1] = bf16_hi(xw[i]); }
+            float db = 0.f, ds = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                db = fmaf(xf[i], wf[i], db);
+                ds += ((bb[j] >> i) & 1u) ? xf[i] : -xf[i];
+            }
+            accb[j] += db;
+            accs[j] += ds;
+        }
+    };
+    int64_t c = lane;
+    for (; c + 32 * (U - 1) < kc; c += 32 * U) {
+        uint4 wv[U];
+        uint4 xv[U][MT];
+        uint32_t bb[U][MT];
+#pragma unroll
+        for (int u = 0; u < U; ++u) wv[u] = ld_stream(wrow + c + 32 * u);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int j = 0; j < MT; ++j) {
+                xv[u][j] = tok[j] >= 0 ? __ldg(x + static_cast<int64_t>(tok[j]) * kc + c + 32 * u) : make_uint4(0, 0, 0, 0);
+                bb[u][j] = bp[j] ? static_cast<uint32_t>(__ldg(bp[j] + c + 32 * u)) : 0u;
+            }
+#pragma unroll
+        for (int u = 0; u < U; ++u) chunk(wv[u], xv[u], bb[u]);
+    }
+    for (; c < kc; c += 32) {
+        uint4 xv[MT];
+        uint32_t bb[MT];
+        const uint4 wv = ld_stream(wrow + c);
+#pragma unroll
+        for (int j = 0; j < MT; ++j) {
+            xv[j] = tok[j] >= 0 ? __ldg(x + static_cast<int64_t>(tok[j]) * kc + c) : make_uint4(0, 0, 0, 0);
+            bb[j] = bp[j] ? static_cast<uint32_t>(__ldg(bp[j] + c)) : 0u;
+        }
+        chunk(wv, xv, bb);
+    }
+#pragma unroll
+    for (int j = 0; j < MT; ++j) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            accb[j] += __shfl_xor_sync(0xffffffffu, accb[j], o);
+            accs[j] += __shfl_xor_sync(0xffffffffu, accs[j], o);
+        }
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int j = 0; j < MT; ++j) {
+            if (j >= M) continue;
+            const int t = g.pos2tok[j];
+            float out = 0.f;
+            if (var[j] >= 0) out = fmaf(alphas[var[j]], accs[j], accb[j]);
+            else if (var[j] == -1) out = accb[j];
+            const int64_t o = static_cast<int64_t>(t) * N + n;
+            if (y_bf16) static_cast<__nv_bfloat16*>(y)[o] = __float2bfloat16_rn(out);
+            else static_cast<float*>(y)[o] = out;
+        }
+    }
+}
+
 bd_status launch_group(const int32_t* ids, int64_t M, int32_t V, const LinearWorkspace& w,
                        cudaStream_t s) {
     int threads = static_cast<int>(round_up(static_cast<size_t>(M), 32));
@@ -232,6 +333,17 @@ bd_status launch_group(const int32_t* ids, int64_t M, int32_t V, const LinearWor
 
 bd_status launch_simt(const LinearArgs& a, const LinearWorkspace& w, cudaStream_t s) {
     const int64_t blocks = (a.N + kSimtWarps - 1) / kSimtWarps;
+    if (a.M <= 4) {
+        const uint4* xx = static_cast<const uint4*>(a.x);
+        const uint4* wb = static_cast<const uint4*>(a.w_base);
+        const int M = static_cast<int>(a.M);
+        const int yb = a.y_dtype == BD_BF16;
+        const unsigned grid = static_cast<unsigned>(blocks);
+        if (a.M == 1) gemv_kernel<1, 4><<<grid, kSimtWarps * 32, 0, s>>>(xx, wb, a.alphas, a.bits, M, a.N, a.K, w.g, a.y, yb);
+        else if (a.M == 2) gemv_kernel<2, 4><<<grid, kSimtWarps * 32, 0, s>>>(xx, wb, a.alphas, a.bits, M, a.N, a.K, w.g, a.y, yb);
+        else gemv_kernel<4, 2><<<grid, kSimtWarps * 32, 0, s>>>(xx, wb, a.alphas, a.bits, M, a.N, a.K, w.g, a.y, yb);
+        return launch_status();
+    }
     simt_linear_kernel<<<static_cast<unsigned>(blocks), kSimtWarps * 32, 0, s>>>(
         static_cast<const uint4*>(a.x), static_cast<const uint4*>(a.w_base), a.alphas, a.bits,
         a.M, a.N, a.K, w.g, a.y, a.y_dtype == BD_BF16);

@@ -150,7 +150,8 @@ def test_prefill_gate(bd, o, path):
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("M,N,K,V", [(1, 8, 32, 1), (37, 100, 96, 3), (5, 129, 64, 0),
                                      (300, 72, 160, 5), (17, 1000, 512, 64), (37, 200, 128, 3),
-                                     (208, 384, 192, 14), (2, 130, 640, 2), (64, 1024, 4096, 14)])
+                                     (208, 384, 192, 14), (2, 130, 640, 2), (64, 1024, 4096, 14),
+                                     (3, 96, 256, 2), (4, 200, 4096, 3)])
 def test_ragged_and_edges(bd, o, path, M, N, K, V):
     g = wl.generator(M * 131 + N * 7 + K + V, DEV)
     wb = wl.base_weights(N, K, g, DEV)
