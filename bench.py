@@ -48,7 +48,7 @@ def parse_args():
     p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--path", default="auto", help="kernel path: auto|simt|decode_tc|prefill_tc")
+    p.add_argument("--path", default="auto", help="kernel path: auto|simt|decode_tc|decode_fold|prefill_tc")
     p.add_argument("--layers", type=int, default=20)
     p.add_argument("--tokens", type=int, default=128)
     p.add_argument("--variants", type=int, default=14)

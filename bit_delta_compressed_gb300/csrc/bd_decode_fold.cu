@@ -1,0 +1,783 @@
+// bd_decode_fold.cu -- folded tensor-core decode path of the fused
+// multi-variant linear.
+//
+// Page: "BitDelta: serving 14 Zen models from one GPU cluster", section
+// "Serving architecture": the base weights are read once and shared by every
+// variant, each variant's delta arrives as packed sign bits and is expanded
+// on chip, and W_eff = W_base + alpha_v * sign(delta_v) never exists in HBM.
+//
+// The base product and the sign product accumulate into ONE tensor-memory
+// accumulator with a column per token (grouped order):
+//   D[n, t] = sum_k W[n,k] (x[t,k] 2^s_t)  +  sum_k s_v[n,k] (alpha_v x[t,k] 2^s_t)
+//   y[t, n] = 2^-s_t D[n, t]
+// where 2^s_t is a per-token power of two (exact) that puts the largest
+// |alpha_v x[t,k]| 2^s_t in [128, 256).  The base operand is the bf16
+// activation row scaled by 2^s_t (exact); the sign operand is alpha_v x 2^s_t
+// written as the sum of two e4m3 terms hi = rn(v), lo = rn(v - hi), which
+// keeps about 8 significant bits of every element (the same order as the
+// bf16 activations themselves).  Folding alpha into the sign operand is what
+// lets both products share one accumulator, so tensor memory holds only
+// pad16(M) accumulator columns and the rest is free for +-1 tiles.
+//
+// One CTA owns 128 output rows (the 128 lanes of tensor memory) and a slice
+// of K (split-K at even 64-column blocks, summed in a fixed order by the CTA
+// that finishes the tile last).  Warps:
+//   * 0, 1, 2 (TMA producers, each with a ring of its own): W_base tiles
+//     (128 x 64 bf16, 128-byte swizzle) from HBM; per 64-column block the
+//     scaled activations X_c (pad16(M) rows) and the sign operand X_p (R rows)
+//     from L2; per pair of blocks one 128-row x 4-word tile of packed bits per
+//     present variant from HBM;
+//   * four issuer groups of five warps.  Group g owns the accumulator columns
+//     of a contiguous run of 16-token chunks (balanced by the grouping
+//     kernel).  Its four expansion warps (one per tensor-memory lane quarter)
+//     turn the bits of the group's entries into e4m3 +-1 tiles in tensor
+//     memory (two buffers) -- one shift and one LOP3 per four weights:
+//     register j = ((w << (7 - j)) & 0x80808080) ^ 0xB8B8B8B8 holds columns
+//     j, j+8, j+16, j+24 of a 32-bit word -- and arrive on a named barrier;
+//     its issuer warp then issues, per 32-column K step, the bf16 base product
+//     over the group's columns and two e4m3 sign products (hi, lo) per entry
+//     (a present variant with tokens in the group's columns; variant runs that
+//     share a chunk are separated by zero rows in X_p).  Groups write
+//     disjoint columns and need no ordering among themselves; the expansion
+//     warps finally read the group's columns and write y = 2^-s_t D.
+// The columns inside each 32-column group of X_p are permuted to match the
+// register layout above.  MMAs are issued by converged warps (elect.sync).
+// Waiting warps poll with one lane that suspends in mbarrier.try_wait, and
+// the sign bits come by TMA: per-thread global loads or polling by whole
+// warps slow the tensor-core issue of the whole SM.
+#include <cuda_fp8.h>
+
+#include "bd_sm100.cuh"
+#include "bd_tc_common.cuh"
+
+namespace bd {
+
+namespace {
+
+constexpr int kBN = 128;                        // output rows per CTA
+constexpr int kBK = 64;                         // K per block
+constexpr int kWMax = 4;                        // W_base ring stages (runtime: 3 or 4)
+constexpr int kXMax = 2;                        // activation ring stages (runtime: 1 or 2)
+constexpr int kBStages = 2;                     // bits ring stages, two 64-column blocks each
+constexpr int kIss = kFoldIssuers;             // issuer groups
+constexpr int kGroupWarps = 5;                  // 4 expansion warps (one per lane quarter) + 1 issuer
+constexpr int kFirstGroup = 3;                  // warps 0, 1, 2: W, activation and bits producers
+constexpr int kThreads = 32 * (kFirstGroup + kIss * kGroupWarps);
+constexpr int kABufs = 2;                       // +-1 tile buffers per group
+constexpr int kACol0 = kFoldMaxCols;            // +-1 tiles after the accumulator
+constexpr int kAEntries = (512 - kFoldMaxCols) / (8 * kABufs);   // entries whose tiles fit
+constexpr int kTmemCols = 512;
+constexpr uint32_t kWaitLimit = 1u << 20;
+constexpr uint32_t kWTile = kBN * 128;
+static_assert(kAEntries >= kFoldMaxEntries, "tensor memory budget");
+
+struct FoldParams {
+    CUtensorMap tm_w;                           // W_base [N, K] bf16, box 128 rows
+    CUtensorMap tm_xc;                          // X_c [Mb, K] bf16, box Mb rows
+    CUtensorMap tm_xp16;                        // X_p [Rmax, 2K] bytes, box 16 rows
+    CUtensorMap tm_xp128;                       // the same, box 128 rows
+    CUtensorMap tm_bits[BITDELTA_MAX_VARIANTS];  // packed bits [N, K/32] u32, box 128 rows x 4 words
+    const SegPlan* plan;
+    const FoldPlan* fold;
+    const int32_t* pos2tok;
+    const int32_t* sexp;                        // [Mb] scale exponent s per grouped position
+    void* y;
+    float* part;                                // [splits][M][N] by grouped position
+    unsigned* tickets;
+    unsigned* status;
+    unsigned* diag;
+    int M, N, K, Mb, Rmax, splits, y_bf16;
+    int wstages, xstages, bslots;               // ring depths; variants per bits stage
+};
+
+__device__ __forceinline__ float pow2i(int e) {        // exact 2^e, e in [-126, 127]
+    return __int_as_float((127 + e) << 23);
+}
+
+// tcgen05.mma issued by one elected lane of a converged warp.
+__device__ __forceinline__ void mma_bf16_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void mma_e4m3_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, 1, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+        "r"(a_tmem), "l"(b), "r"(idesc)
+        : "memory");
+}
+__device__ __forceinline__ void commit_elect(uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+            sm100::smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void store_out(const FoldParams& p, int split, int pos, int tok, int n, float v) {
+    if (p.splits > 1) {
+        p.part[(static_cast<int64_t>(split) * p.M + pos) * p.N + n] = v;
+    } else if (p.y_bf16) {
+        static_cast<__nv_bfloat16*>(p.y)[static_cast<int64_t>(tok) * p.N + n] = __float2bfloat16_rn(v);
+    } else {
+        static_cast<float*>(p.y)[static_cast<int64_t>(tok) * p.N + n] = v;
+    }
+}
+
+__device__ __forceinline__ void named_arrive(int id, int n) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void named_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+constexpr int kGroupThreads = 32 * kGroupWarps;
+constexpr unsigned kFull = 0xffffffffu;
+// Named barrier of group g's +-1 tile buffer b (barrier 0 is __syncthreads).
+__device__ __forceinline__ int group_bar(int g, int b) { return 1 + kABufs * g + b; }
+
+// The issuer warp of a group: per 32-column K step j of block i, wait for the
+// group's tiles (named barrier), then issue the base product over the
+// group's columns and the hi/lo sign products of its entries.  Every barrier
+// is visited on every step, also after an error, so the group never blocks.
+__device__ void group_issue(const FoldParams& p, const FoldPlan& fp, uint32_t tmem, uint32_t abase, int bcol,
+                            int bn, int e0, int ne, int g, int nkb, uint8_t* wring, uint8_t* xring,
+                            uint32_t xs_bytes, uint64_t* w_full, uint64_t* w_empty, uint64_t* x_full,
+                            uint64_t* x_empty, uint64_t* ge, uint64_t* acc_full, uint64_t* drain) {
+    using namespace sm100;
+    const int lane = threadIdx.x & 31;
+    const bool work = bn > 0;
+    const uint32_t idb = idesc_bf16(128, work ? bn : 16);
+    const int Mb = p.Mb;
+    bool ok = true;
+    for (int i = 0; i < nkb; ++i) {
+        const int ws = i % p.wstages, xs = i % p.xstages;
+        for (int j = 0; j < 2; ++j) {
+            named_sync(group_bar(g, j), kGroupThreads);
+            if (ok && j == 0) {
+                ok = warp_wait(&x_full[xs], (i / p.xstages) & 1, kWaitLimit, p.status, 26, p.diag);
+                if (ok) ok = warp_wait(&w_full[ws], (i / p.wstages) & 1, kWaitLimit, p.status, 27, p.diag);
+            }
+            if (!ok) continue;
+            tc_fence_after();
+            if (work) {
+                const uint32_t sw = smem_u32(wring + ws * kWTile);
+                const uint32_t sx = smem_u32(xring + xs * xs_bytes);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int k16 = 2 * j + h;
+                    mma_bf16_ss(tmem + bcol, desc_sw128(sw + 32 * k16), desc_sw128(sx + bcol * 128 + 32 * k16), idb,
+                                (i > 0 || k16 > 0) ? 1u : 0u);
+                }
+                const uint32_t sxp = sx + Mb * 128;
+                const uint32_t abuf = abase + j * 8 * ne;
+                for (int e = e0; e < e0 + ne; ++e) {
+                    const uint32_t d = tmem + fp.e_col[e];
+                    const uint32_t a = abuf + 8 * (e - e0);
+                    const uint32_t brow = sxp + fp.e_row[e] * 128 + 32 * j;
+                    const uint32_t id8 = idesc_e4m3(128, fp.e_n[e]);
+                    mma_e4m3_ts(d, a, desc_sw128(brow), id8);
+                    mma_e4m3_ts(d, a, desc_sw128(brow + 64), id8);
+                }
+                commit_elect(&ge[j]);
+                if (j == 1) {
+                    commit_elect(&x_empty[xs]);
+                    commit_elect(&w_empty[ws]);
+                }
+            } else {
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&ge[j]);
+                    if (j == 1) { mbar_arrive(&x_empty[xs]); mbar_arrive(&w_empty[ws]); }
+                }
+            }
+        }
+    }
+    __syncwarp();
+    if (work) {
+        if (ok) commit_elect(acc_full);
+        commit_elect(drain);                 // completes when every MMA of this warp has
+    } else if (lane == 0) {
+        if (ok) mbar_arrive(acc_full);
+        mbar_arrive(drain);
+    }
+}
+
+// +-1 tile of one 32-column word of sign bits, e4m3: register j holds
+// columns j, j+8, j+16, j+24 (bit 1 -> 0x38 = +1.0, bit 0 -> 0xB8 = -1.0).
+__device__ __forceinline__ void store_signs(uint32_t taddr, uint32_t w) {
+    uint32_t v[8];
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) v[jj] = ((w << (7 - jj)) & 0x80808080u) ^ 0xB8B8B8B8u;
+    sm100::tmem_st8(taddr, v);
+}
+
+// An expansion warp of a group (lane quarter q4): per 32-column K step, wait
+// until the buffer's previous MMAs are done, write the group's +-1 tiles for
+// its 32 rows from the bits tiles that TMA put in shared memory (128 rows x 4
+// words per present variant, two 64-column blocks per stage), and arrive on
+// the group's named barrier; at the end read the group's accumulator columns
+// and write y = 2^-s_t D.
+__device__ void group_expand(const FoldParams& p, const SegPlan& pl, const FoldPlan& fp, uint32_t tmem,
+                             uint32_t abase, int e0, int ne, int g, int q4, int n0, int nkb, uint64_t* ge,
+                             const uint8_t* bring, uint32_t bstage_bytes, uint64_t* b_full, uint64_t* b_empty,
+                             uint64_t* acc_full, const int32_t* tok_s, const float* scale_s, int split, int bcol,
+                             int bn) {
+    using namespace sm100;
+    const int lane = threadIdx.x & 31;
+    const int r = 32 * q4 + lane;
+    const int n = n0 + r;
+    const bool row_ok = n < p.N;
+    const uint32_t lane_addr = static_cast<uint32_t>(32 * q4) << 16;
+    bool ok = true;
+    for (int i = 0; i < nkb; ++i) {
+        const int m = i >> 1, half = i & 1, bs = m & 1;
+        if (ok && half == 0) ok = warp_wait(&b_full[bs], (m >> 1) & 1, kWaitLimit, p.status, 31, p.diag);
+        const uint32_t* words = reinterpret_cast<const uint32_t*>(bring + bs * bstage_bytes) + r * 4 + 2 * half;
+        for (int j = 0; j < 2; ++j) {
+            if (ok) ok = warp_wait(&ge[j], (i & 1) ^ 1, kWaitLimit, p.status, 28, p.diag);
+            if (ok) {
+                tc_fence_after();
+                const uint32_t col = abase + lane_addr + j * 8 * ne;
+                for (int k = 0; k < ne; ++k)
+                    store_signs(col + 8 * k, words[fp.e_slot[e0 + k] * 512 + j]);
+                tmem_st_wait();
+            }
+            tc_fence_before();
+            named_arrive(group_bar(g, j), kGroupThreads);
+        }
+        if (half == 1 || i == nkb - 1) {             // done with this bits stage
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&b_empty[bs]);
+        }
+    }
+    // ---- epilogue: y = 2^-s_t D over the group's columns ----
+    if (ok) ok = warp_wait(acc_full, 0, kWaitLimit, p.status, 29, p.diag);
+    if (!ok) return;
+    tc_fence_after();
+    const int n_valid = pl.M - pl.n_invalid;
+    for (int c0 = bcol; c0 < bcol + bn; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(tmem + lane_addr + c0, v);
+        tmem_ld_wait();
+        if (row_ok) {
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+                const int pos = c0 + t;
+                if (pos >= p.M) break;
+                const float val = pos < n_valid ? __uint_as_float(v[t]) * scale_s[pos] : 0.f;
+                store_out(p, split, pos, tok_s[pos], n, val);
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) fold_decode_kernel(const __grid_constant__ FoldParams p) {
+    using namespace sm100;
+    extern __shared__ uint8_t dsmem[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
+    __shared__ uint64_t w_full[kWMax], w_empty[kWMax], x_full[kXMax], x_empty[kXMax];
+    __shared__ uint64_t b_full[kBStages], b_empty[kBStages];
+    __shared__ uint64_t g_empty[kIss][kABufs], acc_full, drain;
+    __shared__ uint32_t tmem_base;
+    __shared__ SegPlan pl;
+    __shared__ FoldPlan fp;
+    __shared__ int last_cta;
+    __shared__ int32_t tok_s[kFoldMaxCols];
+    __shared__ float scale_s[kFoldMaxCols];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int Mb = p.Mb;
+    const uint32_t xs_bytes = static_cast<uint32_t>(Mb + p.Rmax) * 128u;
+    const uint32_t bstage_bytes = static_cast<uint32_t>(p.bslots) * 2048u;
+    uint8_t* wring = base;
+    uint8_t* bring = wring + p.wstages * kWTile;
+    uint8_t* xring = bring + kBStages * bstage_bytes;
+    const int tile = blockIdx.x / p.splits, split = blockIdx.x % p.splits;
+    const int n0 = tile * kBN;
+    // K slices are cut at even 64-column blocks, so every bits copy (two
+    // blocks, 16 bytes a row) starts on a 16-byte boundary
+    const int kb_total = p.K / kBK;
+    const int npairs = (kb_total + 1) / 2;
+    const int kb0 = 2 * static_cast<int>(static_cast<int64_t>(split) * npairs / p.splits);
+    const int kb1 = min(kb_total, 2 * static_cast<int>(static_cast<int64_t>(split + 1) * npairs / p.splits));
+    const int nkb = kb1 - kb0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kWMax; ++s) { mbar_init(&w_full[s], 1); mbar_init(&w_empty[s], kIss); }
+        for (int s = 0; s < kXMax; ++s) { mbar_init(&x_full[s], 1); mbar_init(&x_empty[s], kIss); }
+        for (int s = 0; s < kBStages; ++s) { mbar_init(&b_full[s], 1); mbar_init(&b_empty[s], 4 * kIss); }
+        for (int g = 0; g < kIss; ++g)
+            for (int b = 0; b < kABufs; ++b) mbar_init(&g_empty[g][b], 1);
+        mbar_init(&acc_full, kIss);
+        mbar_init(&drain, kIss);
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(&tmem_base, kTmemCols);
+    // everything above overlaps the staging kernel; its outputs are read below
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    {
+        const int* src = reinterpret_cast<const int*>(p.plan);
+        int* dst = reinterpret_cast<int*>(&pl);
+        for (int i = threadIdx.x; i < static_cast<int>(sizeof(SegPlan) / 4); i += blockDim.x) dst[i] = src[i];
+        const int* fsrc = reinterpret_cast<const int*>(p.fold);
+        int* fdst = reinterpret_cast<int*>(&fp);
+        for (int i = threadIdx.x; i < static_cast<int>(sizeof(FoldPlan) / 4); i += blockDim.x) fdst[i] = fsrc[i];
+    }
+    for (int q = threadIdx.x; q < Mb; q += blockDim.x) {
+        tok_s[q] = q < p.M ? p.pos2tok[q] : -1;
+        scale_s[q] = pow2i(-p.sexp[q]);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+    // the host only picks this kernel when the plan fits; anything else is a bug
+    const bool plan_ok = fp.ok != 0 && fp.R <= p.Rmax && fp.C * 16 == Mb && pl.D <= kFoldMaxSlots &&
+                         fp.n_entries <= kAEntries && pl.D <= p.bslots;
+    if (!plan_ok && threadIdx.x == 0) report(p.status, BD_ERR_UNSUPPORTED);
+
+    if (!plan_ok) {
+        // nothing was issued; fall through to the teardown
+    } else if (warp == 0) {
+        // ---------------- TMA producer: W_base tiles (HBM) ----------------
+        // W and the activations have rings of their own, so the W stream runs
+        // its full depth ahead whatever the depth of the activation ring.
+        if (lane == 0) {
+            prefetch_tensormap(&p.tm_w);
+            int issued = 0;
+            for (int i = 0; i < nkb; ++i) {
+                const int ws = i % p.wstages;
+                if (!mbar_wait(&w_empty[ws], ((i / p.wstages) & 1) ^ 1, kWaitLimit, p.status, 21, p.diag)) break;
+                mbar_expect_tx(&w_full[ws], kWTile);
+                tma_load_2d(wring + ws * kWTile, &p.tm_w, &w_full[ws], (kb0 + i) * kBK, n0);
+                issued = i + 1;
+            }
+            // wait (bounded) until every load issued has landed, so no copy is
+            // still writing shared memory when the CTA exits
+            for (int s = 0; s < p.wstages && s < issued; ++s) {
+                const int last = issued - 1 - ((issued - 1 - s) % p.wstages);
+                mbar_wait(&w_full[s], (last / p.wstages) & 1, kWaitLimit, p.status, 23, p.diag);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- TMA producer: activations (L2) ----------------
+        if (lane == 0) {
+            prefetch_tensormap(&p.tm_xc);
+            prefetch_tensormap(&p.tm_xp16);
+            prefetch_tensormap(&p.tm_xp128);
+            const int R = fp.R;
+            int issued = 0;
+            for (int i = 0; i < nkb; ++i) {
+                const int kb = kb0 + i;
+                const int xs = i % p.xstages;
+                if (!mbar_wait(&x_empty[xs], ((i / p.xstages) & 1) ^ 1, kWaitLimit, p.status, 22, p.diag)) break;
+                uint8_t* sx = xring + xs * xs_bytes;
+                mbar_expect_tx(&x_full[xs], static_cast<uint32_t>(Mb + R) * 128u);
+                tma_load_2d(sx, &p.tm_xc, &x_full[xs], kb * kBK, 0);
+                uint8_t* sxp = sx + Mb * 128;
+                int r = 0;
+                for (; r + 128 <= R; r += 128) tma_load_2d(sxp + r * 128, &p.tm_xp128, &x_full[xs], kb * 128, r);
+                for (; r < R; r += 16) tma_load_2d(sxp + r * 128, &p.tm_xp16, &x_full[xs], kb * 128, r);
+                issued = i + 1;
+            }
+            for (int s = 0; s < p.xstages && s < issued; ++s) {
+                const int last = issued - 1 - ((issued - 1 - s) % p.xstages);
+                mbar_wait(&x_full[s], (last / p.xstages) & 1, kWaitLimit, p.status, 24, p.diag);
+            }
+        }
+    } else if (warp == 2) {
+        // ---------------- TMA producer: sign bits (HBM) ----------------
+        // one 128-row x 4-word tile per present variant and pair of blocks
+        if (lane == 0) {
+            const int D = pl.D;
+            for (int d = 0; d < D; ++d) prefetch_tensormap(&p.tm_bits[pl.var[d]]);
+            const int np = (nkb + 1) / 2;
+            int issued = 0;
+            for (int m = 0; m < np; ++m) {
+                const int bs = m % kBStages;
+                if (!mbar_wait(&b_empty[bs], ((m / kBStages) & 1) ^ 1, kWaitLimit, p.status, 32, p.diag)) break;
+                if (D == 0) { mbar_arrive(&b_full[bs]); issued = m + 1; continue; }
+                mbar_expect_tx(&b_full[bs], static_cast<uint32_t>(D) * 2048u);
+                uint8_t* sb = bring + bs * bstage_bytes;
+                for (int d = 0; d < D; ++d)
+                    tma_load_2d(sb + d * 2048, &p.tm_bits[pl.var[d]], &b_full[bs], 2 * (kb0 + 2 * m), n0);
+                issued = m + 1;
+            }
+            for (int s = 0; s < kBStages && s < issued; ++s) {
+                const int last = issued - 1 - ((issued - 1 - s) % kBStages);
+                mbar_wait(&b_full[s], (last / kBStages) & 1, kWaitLimit, p.status, 33, p.diag);
+            }
+        }
+    } else {
+        // ---------------- issuer groups ----------------
+        // Group g: four expansion warps (one per tensor-memory lane quarter)
+        // build the +-1 tiles of the group's own entries, then arrive on a
+        // named barrier; the group's issuer warp waits on it and issues the
+        // group's MMAs.  Each group owns a disjoint run of accumulator
+        // columns, so groups never wait for one another.
+        const int g = (warp - kFirstGroup) / kGroupWarps;
+        const int gw = (warp - kFirstGroup) % kGroupWarps;
+        const int bcol = fp.iss_col[g], bn = fp.iss_n[g];
+        const int e0 = fp.iss_e0[g], ne = fp.iss_ne[g];
+        int a0 = 0;                                 // first +-1 tile column of this group
+        for (int h = 0; h < g; ++h) a0 += 8 * kABufs * fp.iss_ne[h];
+        const uint32_t abase = tmem + kACol0 + a0;
+        if (gw == kGroupWarps - 1)
+            group_issue(p, fp, tmem, abase, bcol, bn, e0, ne, g, nkb, wring, xring, xs_bytes, w_full, w_empty,
+                        x_full, x_empty, g_empty[g], &acc_full, &drain);
+        else
+            group_expand(p, pl, fp, tmem, abase, e0, ne, g, warp % 4, n0, nkb, g_empty[g], bring, bstage_bytes,
+                         b_full, b_empty, &acc_full, tok_s, scale_s, split, bcol, bn);
+    }
+
+    __syncthreads();
+    if (plan_ok && p.splits > 1) {
+        // deterministic split-K reduction by the CTA that finishes the tile last
+        if (threadIdx.x == 0) {
+            __threadfence();
+            const unsigned t = atomicAdd(&p.tickets[tile], 1u);
+            last_cta = (t == static_cast<unsigned>(p.splits - 1));
+        }
+        __syncthreads();
+        if (last_cta) {
+            __threadfence();
+            const int rows = min(kBN, p.N - n0);
+            for (int idx = threadIdx.x; idx < p.M * rows; idx += blockDim.x) {
+                const int pos = idx / rows, rr = idx % rows;
+                float acc = 0.f;
+                for (int s = 0; s < p.splits; ++s)
+                    acc += __ldcg(p.part + (static_cast<int64_t>(s) * p.M + pos) * p.N + n0 + rr);
+                const int64_t o = static_cast<int64_t>(tok_s[pos]) * p.N + n0 + rr;
+                if (p.y_bf16) static_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(acc);
+                else static_cast<float*>(p.y)[o] = acc;
+            }
+            if (threadIdx.x == 0) p.tickets[tile] = 0u;
+        }
+    }
+    if (warp == 0) {
+        // every MMA this CTA issued has completed before its tensor memory is freed
+        if (plan_ok) mbar_wait(&drain, 0, kWaitLimit, p.status, 30, p.diag);
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Staging for one linear (one block per staged row):
+//   X_c [Mb, K] bf16: grouped order, row p = x[t] * 2^s_t (zero rows past the
+//       valid tokens);
+//   X_p [R, 2K] bytes: entry rows of the plan; row j of entry e holds, if
+//       grouped position e_col + j is a token of the entry's variant v,
+//       alpha_v x[t] 2^s_t as e4m3 hi and lo, per 64-column block 64 bytes
+//       of hi then 64 of lo, byte 32w + 4j + b of a half holding column
+//       32w + j + 8b; otherwise zeros;
+//   s_t = 7 - floor(log2(|alpha_v| max_k |x[t,k]|)) (0 for base-model
+//       tokens, zero rows and zero alpha), clamped to [-64, 64];
+//   the split-K tickets zeroed.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t to_e4m3(float v) {
+    return static_cast<uint32_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+}
+__device__ __forceinline__ float from_e4m3(uint32_t b) {
+    __half_raw hr = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(b), __NV_E4M3);
+    return __half2float(__half(hr));
+}
+
+// Largest |x| of a bf16 row (bf16 bit patterns without the sign order like
+// magnitudes), reduced over the block.
+__device__ float row_absmax(const uint4* __restrict__ src, int64_t vec_per_row) {
+    __shared__ uint32_t red[8];
+    uint32_t mx = 0;
+    for (int64_t i = threadIdx.x; i < vec_per_row; i += blockDim.x) {
+        const uint4 v = __ldg(src + i);
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mx = max(mx, max(w4[k] & 0x7FFFu, (w4[k] >> 16) & 0x7FFFu));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    uint32_t all = 0;
+    for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) all = max(all, red[i]);
+    return __uint_as_float(all << 16);
+}
+
+__device__ __forceinline__ int scale_exponent(float alpha, float xmax) {
+    const float prod = fabsf(alpha) * xmax;
+    if (!(prod > 0.f) || !(prod < 3.0e38f)) return 0;
+    const int biased = static_cast<int>((__float_as_uint(prod) >> 23) & 0xFF);
+    const int e = biased > 0 ? biased - 127 : -127;
+    return max(-64, min(64, 7 - e));
+}
+
+__global__ void __launch_bounds__(256) fold_prep_kernel(const uint4* __restrict__ x, int K, int M, int Mb,
+                                                        const float* __restrict__ alphas,
+                                                        const SegPlan* __restrict__ plan,
+                                                        const FoldPlan* __restrict__ fold,
+                                                        const int32_t* __restrict__ pos2tok,
+                                                        const int32_t* __restrict__ pos_var,
+                                                        int32_t* __restrict__ sexp, uint4* __restrict__ xc,
+                                                        uint4* __restrict__ xp, unsigned* tickets, int n_tickets) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int rr = blockIdx.x;
+    const int64_t vec_per_row = K / 8;
+    if (rr == 0)
+        for (int i = threadIdx.x; i < n_tickets; i += blockDim.x) tickets[i] = 0u;
+    const int n_valid = M - plan->n_invalid;
+    if (rr < Mb) {
+        const int pos = rr;
+        const int tok = pos < n_valid ? pos2tok[pos] : -1;
+        const int var = pos < n_valid ? pos_var[pos] : -2;
+        uint4* dst = xc + static_cast<int64_t>(pos) * vec_per_row;
+        if (tok < 0) {
+            for (int64_t i = threadIdx.x; i < vec_per_row; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
+            if (threadIdx.x == 0) sexp[pos] = 0;
+            return;
+        }
+        const uint4* src = x + static_cast<int64_t>(tok) * vec_per_row;
+        const int s = var >= 0 ? scale_exponent(alphas[var], row_absmax(src, vec_per_row)) : 0;
+        if (threadIdx.x == 0) sexp[pos] = s;
+        const float sc = pow2i(s);
+        for (int64_t i = threadIdx.x; i < vec_per_row; i += blockDim.x) {
+            const uint4 v = __ldg(src + i);
+            uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+            if (s != 0) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const __nv_bfloat162 pr = __floats2bfloat162_rn(bf16_lo(w4[k]) * sc, bf16_hi(w4[k]) * sc);
+                    w4[k] = *reinterpret_cast<const uint32_t*>(&pr);
+                }
+            }
+            dst[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+        return;
+    }
+    const int r = rr - Mb;
+    if (r >= fold->R) return;
+    int tok = -1, var = -1;
+    for (int e = 0; e < fold->n_entries; ++e) {
+        const int row0 = fold->e_row[e];
+        if (r >= row0 && r < row0 + fold->e_n[e]) {
+            const int pos = fold->e_col[e] + (r - row0);
+            const int d = fold->e_slot[e];
+            if (pos >= plan->off[d] && pos < plan->off[d] + plan->cnt[d]) {
+                tok = pos2tok[pos];
+                var = plan->var[d];
+            }
+            break;
+        }
+    }
+    uint4* dst = xp + static_cast<int64_t>(r) * vec_per_row;    // 2K bytes: hi and lo per block
+    if (tok < 0) {
+        for (int64_t i = threadIdx.x; i < vec_per_row; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
+        return;
+    }
+    const uint4* src = x + static_cast<int64_t>(tok) * vec_per_row;
+    const float alpha = alphas[var];
+    const int s = scale_exponent(alpha, row_absmax(src, vec_per_row));
+    const float sc = pow2i(s);
+    for (int blk = threadIdx.x; blk < K / 64; blk += blockDim.x) {
+        uint32_t w[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint4 v = __ldg(src + 8 * blk + i);
+            w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+        }
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) { hi[i] = 0; lo[i] = 0; }
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {                    // source column c of the block
+            const float xv = (c & 1) ? bf16_hi(w[c >> 1]) : bf16_lo(w[c >> 1]);
+            const float v = (alpha * xv) * sc;
+            const uint32_t h8 = to_e4m3(v);
+            const uint32_t l8 = to_e4m3(v - from_e4m3(h8));
+            const int wd = c >> 5, cc = c & 31;            // word, column within it
+            const int byte = 32 * wd + 4 * (cc & 7) + (cc >> 3);
+            hi[byte >> 2] |= h8 << (8 * (byte & 3));
+            lo[byte >> 2] |= l8 << (8 * (byte & 3));
+        }
+        uint4* o = dst + 8 * blk;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            o[i] = make_uint4(hi[4 * i], hi[4 * i + 1], hi[4 * i + 2], hi[4 * i + 3]);
+            o[4 + i] = make_uint4(lo[4 * i], lo[4 * i + 1], lo[4 * i + 2], lo[4 * i + 3]);
+        }
+    }
+}
+
+int fold_dmax(int64_t M, int32_t V) {
+    int64_t d = V < M ? V : M;
+    return static_cast<int>(d < kFoldMaxSlots ? d : kFoldMaxSlots);
+}
+
+// Sign-operand rows: the entries' chunks, at most (chunks + variants - 1)
+// of 16 rows (variant runs meet other runs only at their end chunks).
+int fold_rmax(int64_t M, int32_t V) {
+    const int r = 16 * (pad16(static_cast<int>(M)) / 16 + fold_dmax(M, V) - 1);
+    return r > 16 ? r : 16;
+}
+
+// K slices per row tile (in pairs of 64-column blocks): minimise waves x
+// (fixed per-CTA cost + blocks per slice x time per block) + the split-K
+// reduction, which the last CTA of a tile does alone (M x 128 partials per
+// slice at ~100 GB/s).  The time per block is the larger of its HBM time (W
+// tile + one bits tile per variant at ~45 GB/s per SM) and its MMA issue
+// time (~55 cycles per MMA per issuer warp at ~2 GHz).
+int fold_splits(int64_t n_tiles, int kb_total, int sms, int dmax, int64_t M) {
+    const double hbm_us = (16.0 + dmax) * 1024.0 / 45.0e3;
+    const int entries = (dmax + kIss - 1) / kIss + 1;
+    const double issue_us = 2.0 * (2 + 2 * entries) * 55.0 / 2000.0;
+    const double kb_us = hbm_us > issue_us ? hbm_us : issue_us;
+    const double fixed_us = 4.0;
+    const double reduce_us_per_split = static_cast<double>(M) * kBN * 4.0 / 100.0e3;
+    const int npairs = (kb_total + 1) / 2;
+    int best = 1;
+    double best_t = 1e30;
+    for (int s = 1; s <= 32 && s <= npairs; ++s) {
+        const int64_t waves = (n_tiles * s + sms - 1) / sms;
+        const double t = static_cast<double>(waves) * (fixed_us + 2 * ((npairs + s - 1) / s) * kb_us) +
+                         (s > 1 ? s * reduce_us_per_split : 0.0);
+        if (t < best_t * 0.98) { best_t = t; best = s; }
+    }
+    return best;
+}
+
+// Shared-memory plan of one launch: ring depths that fit next to the static
+// shared memory (about 4 KB) under the 227 KB limit.
+struct FoldSmem {
+    int wstages, xstages, bslots, bytes;
+};
+FoldSmem fold_smem(int Mb, int rmax, int dmax) {
+    FoldSmem f;
+    f.bslots = dmax > 0 ? dmax : 1;
+    const int budget = 227 * 1024 - 4096;
+    const int bits = kBStages * f.bslots * 2048;
+    const int xs = (Mb + rmax) * 128;
+    for (f.xstages = kXMax; f.xstages >= 1; --f.xstages)
+        for (f.wstages = kWMax; f.wstages >= 3; --f.wstages) {
+            f.bytes = f.wstages * static_cast<int>(kWTile) + bits + f.xstages * xs + 1024;
+            if (f.bytes <= budget) return f;
+        }
+    f.wstages = 0;                               // does not fit
+    return f;
+}
+
+struct FoldScratch {
+    uint16_t* xc;
+    uint8_t* xp;
+    int32_t* sexp;
+    float* part;
+    unsigned* tickets;
+    size_t bytes;
+};
+
+FoldScratch fold_scratch(void* base, int64_t M, int64_t N, int64_t K, int32_t V, int splits) {
+    FoldScratch d{};
+    char* p = static_cast<char*>(base);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        char* r = p ? p + off : nullptr;
+        off += round_up(bytes, kAlign);
+        return r;
+    };
+    const int Mb = pad16(static_cast<int>(M));
+    d.xc = reinterpret_cast<uint16_t*>(take(static_cast<size_t>(Mb) * K * 2));
+    d.xp = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(fold_rmax(M, V)) * K * 2));
+    d.sexp = reinterpret_cast<int32_t*>(take(static_cast<size_t>(Mb) * 4));
+    const int64_t n_tiles = (N + kBN - 1) / kBN;
+    d.part = splits > 1 ? reinterpret_cast<float*>(take(static_cast<size_t>(splits) * M * N * 4)) : nullptr;
+    d.tickets = reinterpret_cast<unsigned*>(take(static_cast<size_t>(n_tiles) * 4));
+    d.bytes = off;
+    return d;
+}
+
+int splits_for(int64_t M, int64_t N, int64_t K, int32_t V) {
+    const int64_t n_tiles = (N + kBN - 1) / kBN;
+    return fold_splits(n_tiles, static_cast<int>(K / kBK), sm_count(), fold_dmax(M, V), M);
+}
+
+}  // namespace
+
+bool decode_fold_supported(const LinearArgs& a) {
+    return a.M >= 1 && pad16(static_cast<int>(a.M > 4096 ? 4096 : a.M)) <= kFoldMaxCols &&
+           (a.V < a.M ? a.V : a.M) <= kFoldMaxSlots && a.K % kBK == 0 && a.K >= kBK && a.N >= 1 &&
+           a.N < (int64_t(1) << 31) && a.K < (int64_t(1) << 31);
+}
+
+size_t decode_fold_scratch_bytes(int64_t M, int64_t N, int64_t K, int32_t V) {
+    if (M < 1 || pad16(static_cast<int>(M > 4096 ? 4096 : M)) > kFoldMaxCols || K % kBK != 0) return 0;
+    return fold_scratch(nullptr, M, N, K, V, splits_for(M, N, K, V)).bytes;
+}
+
+bd_status launch_decode_fold(const LinearArgs& a, const LinearWorkspace& w, cudaStream_t s) {
+    const int M = static_cast<int>(a.M), N = static_cast<int>(a.N), K = static_cast<int>(a.K);
+    const int Mb = pad16(M);
+    const int64_t n_tiles = (a.N + kBN - 1) / kBN;
+    const int splits = splits_for(a.M, a.N, a.K, a.V);
+    FoldScratch sc = fold_scratch(w.tc_scratch, a.M, a.N, a.K, a.V, splits);
+    if (sc.bytes > w.tc_bytes) return BD_ERR_WORKSPACE;
+    const int rmax = fold_rmax(a.M, a.V);
+
+    fold_prep_kernel<<<Mb + rmax, 256, 0, s>>>(static_cast<const uint4*>(a.x), K, M, Mb, a.alphas, w.g.plan,
+                                              w.g.fold, w.g.pos2tok, w.g.pos_var, sc.sexp,
+                                              reinterpret_cast<uint4*>(sc.xc), reinterpret_cast<uint4*>(sc.xp),
+                                              sc.tickets, splits > 1 ? static_cast<int>(n_tiles) : 0);
+    if (launch_status() != BD_OK) return BD_ERR_CUDA;
+
+    FoldParams p;
+    memset(&p, 0, sizeof p);
+    if (!make_tmap_bf16_sw128(&p.tm_w, a.w_base, a.N, a.K, kBN) ||
+        !make_tmap_bf16_sw128(&p.tm_xc, sc.xc, Mb, a.K, Mb) ||
+        !make_tmap_u8_sw128(&p.tm_xp16, sc.xp, rmax, 2 * a.K, 16) ||
+        !make_tmap_u8_sw128(&p.tm_xp128, sc.xp, rmax, 2 * a.K, 128))
+        return BD_ERR_CUDA;
+    for (int v = 0; v < a.V; ++v)
+        if (!make_tmap_bits(&p.tm_bits[v], a.bits.p[v], a.N, a.K / 32, kBN)) return BD_ERR_CUDA;
+    p.plan = w.g.plan;
+    p.fold = w.g.fold;
+    p.pos2tok = w.g.pos2tok;
+    p.sexp = sc.sexp;
+    p.y = a.y;
+    p.part = sc.part;
+    p.tickets = sc.tickets;
+    p.status = w.status;
+    p.diag = w.status + 2;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.Mb = Mb;
+    p.Rmax = rmax;
+    p.splits = splits;
+    p.y_bf16 = (a.y_dtype == BD_BF16);
+    const FoldSmem fs = fold_smem(Mb, rmax, fold_dmax(a.M, a.V));
+    if (fs.wstages == 0) return BD_ERR_UNSUPPORTED;
+    p.wstages = fs.wstages;
+    p.xstages = fs.xstages;
+    p.bslots = fs.bslots;
+    const int smem = fs.bytes;
+    if (!set_smem_attr(reinterpret_cast<const void*>(fold_decode_kernel), smem, 2)) return BD_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(n_tiles * splits));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, fold_decode_kernel, p) != cudaSuccess) return BD_ERR_CUDA;
+    return launch_status();
+}
+
+}  // namespace bd

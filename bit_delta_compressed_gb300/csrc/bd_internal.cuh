@@ -71,12 +71,34 @@ struct SegPlan {
     int32_t group_first[kMaxGroups + 1];          // present-index range of each pass
 };
 
+// Issue plan of the folded tensor-core decode kernel, also written by the
+// grouping kernel.  The accumulator has one column per grouped position
+// (pad16(M) columns, 16-column chunks); issuer warp i owns the chunk range
+// [iss_col[i], iss_col[i] + iss_n[i]) and issues, per K step, the base
+// product over its range plus one "entry" per present variant whose tokens
+// fall inside it.  Entry e covers columns [e_col, e_col + e_n) with rows
+// [e_row, e_row + e_n) of the sign operand (rows of other variants' tokens
+// are zero there) and the +-1 tile of present variant e_slot.
+constexpr int kFoldIssuers = 4;
+constexpr int kFoldMaxSlots = 16;                       // present variants
+constexpr int kFoldMaxEntries = kFoldMaxSlots + kFoldIssuers;
+constexpr int kFoldMaxCols = 128;                       // pad16(M)
+struct FoldPlan {
+    int32_t ok;                                   // 1 if the batch fits the folded kernel
+    int32_t C;                                    // chunks of 16 columns
+    int32_t R;                                    // rows of the sign operand (multiple of 16)
+    int32_t n_entries;
+    int32_t iss_col[kFoldIssuers], iss_n[kFoldIssuers], iss_e0[kFoldIssuers], iss_ne[kFoldIssuers];
+    int32_t e_col[kFoldMaxEntries], e_n[kFoldMaxEntries], e_slot[kFoldMaxEntries], e_row[kFoldMaxEntries];
+};
+
 struct GroupView {
     int32_t* counts;     // [V + 2]: bucket 0 = id -1 (base), 1..V = variants, V+1 = invalid
     int32_t* offsets;    // [V + 3]: exclusive prefix of counts
     int32_t* pos2tok;    // [M]: grouped position -> original token
     int32_t* pos_var;    // [M]: grouped position -> variant id (-1 base, -2 invalid)
     SegPlan* plan;
+    FoldPlan* fold;
 };
 
 __host__ __device__ inline int pad16(int v) { return (v + 15) & ~15; }

@@ -35,6 +35,7 @@ LinearWorkspace linear_workspace_layout(void* base, int64_t M, int64_t N, int64_
     w.g.pos2tok = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (m ? m : 1)));
     w.g.pos_var = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (m ? m : 1)));
     w.g.plan = reinterpret_cast<SegPlan*>(take(sizeof(SegPlan)));
+    w.g.fold = reinterpret_cast<FoldPlan*>(take(sizeof(FoldPlan)));
     w.group_end = off;
     w.tc_bytes = tc_scratch_bytes(M, N, K, V);
     w.tc_scratch = w.tc_bytes ? take(w.tc_bytes) : nullptr;
@@ -53,6 +54,73 @@ namespace {
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int bucket_of(int32_t id, int V) {
     return (id >= -1 && id < V) ? id + 1 : V + 1;
+}
+
+// Issue plan of the folded decode kernel (one thread).  The 16-column chunks
+// of the accumulator are cut into kFoldIssuers contiguous ranges so that the
+// largest per-range MMA count per K step -- 2 base products plus 2 (hi, lo)
+// per variant touching the range -- is as small as possible (a tiny dynamic
+// programme over at most 8 chunks).
+__device__ void fold_plan(const SegPlan& pl, int M, FoldPlan* fp) {
+    constexpr int I = kFoldIssuers;
+    constexpr int CM = kFoldMaxCols / 16;
+    const int C = pad16(M) / 16;
+    fp->ok = 0;
+    fp->C = C;
+    fp->R = 0;
+    fp->n_entries = 0;
+    for (int i = 0; i < I; ++i) { fp->iss_col[i] = 0; fp->iss_n[i] = 0; fp->iss_e0[i] = 0; fp->iss_ne[i] = 0; }
+    if (C > CM || pl.D > kFoldMaxSlots) return;
+    uint32_t mask[CM];
+    for (int c = 0; c < CM; ++c) mask[c] = 0;
+    for (int d = 0; d < pl.D; ++d) {
+        const int c0 = pl.off[d] / 16, c1 = (pl.off[d] + pl.cnt[d] - 1) / 16;
+        for (int c = c0; c <= c1; ++c) mask[c] |= 1u << d;
+    }
+    auto cost = [&](int a, int b) {
+        if (b <= a) return 0;
+        uint32_t m = 0;
+        for (int c = a; c < b; ++c) m |= mask[c];
+        return 2 + 2 * __popc(m);
+    };
+    constexpr int kBig = 1 << 20;
+    int f[I + 1][CM + 1], arg[I + 1][CM + 1];
+    for (int c = 0; c <= C; ++c) { f[0][c] = c == 0 ? 0 : kBig; arg[0][c] = 0; }
+    for (int i = 1; i <= I; ++i)
+        for (int c = 0; c <= C; ++c) {
+            int best = kBig, ba = 0;
+            for (int a = 0; a <= c; ++a) {
+                const int v = max(f[i - 1][a], cost(a, c));
+                if (v < best) { best = v; ba = a; }
+            }
+            f[i][c] = best;
+            arg[i][c] = ba;
+        }
+    int bnd[I + 1];
+    bnd[I] = C;
+    for (int i = I; i >= 1; --i) bnd[i - 1] = arg[i][bnd[i]];
+    int e = 0, row = 0;
+    for (int i = 0; i < I; ++i) {
+        const int a = bnd[i], b = bnd[i + 1];
+        fp->iss_col[i] = 16 * a;
+        fp->iss_n[i] = 16 * (b - a);
+        fp->iss_e0[i] = e;
+        for (int d = 0; d < pl.D && b > a; ++d) {
+            const int c0 = pl.off[d] / 16, c1 = (pl.off[d] + pl.cnt[d] - 1) / 16;
+            const int cs = max(c0, a), ce = min(c1, b - 1);
+            if (cs > ce) continue;
+            fp->e_col[e] = 16 * cs;
+            fp->e_n[e] = 16 * (ce - cs + 1);
+            fp->e_slot[e] = d;
+            fp->e_row[e] = row;
+            row += 16 * (ce - cs + 1);
+            ++e;
+        }
+        fp->iss_ne[i] = e - fp->iss_e0[i];
+    }
+    fp->n_entries = e;
+    fp->R = row;
+    fp->ok = 1;
 }
 
 __global__ void __launch_bounds__(1024) group_kernel(const int32_t* __restrict__ ids, int M, int V,
@@ -112,6 +180,7 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t* __restrict__
         pl->P = rows;
         pl->n_groups = groups + 1;
         pl->group_first[groups + 1] = d;
+        fold_plan(*pl, M, g.fold);
     }
     __syncthreads();
     for (int s0 = 0; s0 < M; s0 += blockDim.x) {
@@ -405,9 +474,11 @@ bd_status prepare(const void* x, int64_t M, int64_t N, int64_t K, const void* w_
     a.y = y;
     a.y_dtype = y_dtype;
     if (path == BD_PATH_AUTO) path = choose_path(a);
-    if (path != BD_PATH_SIMT && path != BD_PATH_DECODE_TC && path != BD_PATH_PREFILL_TC)
+    if (path != BD_PATH_SIMT && path != BD_PATH_DECODE_TC && path != BD_PATH_PREFILL_TC &&
+        path != BD_PATH_DECODE_FOLD)
         return BD_ERR_UNSUPPORTED;
     if (path == BD_PATH_DECODE_TC && !decode_tc_supported(a)) return BD_ERR_UNSUPPORTED;
+    if (path == BD_PATH_DECODE_FOLD && !decode_fold_supported(a)) return BD_ERR_UNSUPPORTED;
     if (path == BD_PATH_PREFILL_TC && !prefill_tc_supported(a)) return BD_ERR_UNSUPPORTED;
     return BD_OK;
 }
@@ -416,6 +487,7 @@ bd_status launch_path(bd_path path, const LinearArgs& a, const LinearWorkspace& 
                       cudaStream_t s) {
     switch (path) {
         case BD_PATH_DECODE_TC: return launch_decode_tc(a, w, s);
+        case BD_PATH_DECODE_FOLD: return launch_decode_fold(a, w, s);
         case BD_PATH_PREFILL_TC: return launch_prefill_tc(a, w, s);
         default: return launch_simt(a, w, s);
     }

@@ -30,6 +30,9 @@ size_t tc_scratch_bytes(int64_t M, int64_t N, int64_t K, int32_t V);
 bd_path choose_path(const LinearArgs& a);
 bool decode_tc_supported(const LinearArgs& a);
 bool prefill_tc_supported(const LinearArgs& a);
+bool decode_fold_supported(const LinearArgs& a);
+size_t decode_fold_scratch_bytes(int64_t M, int64_t N, int64_t K, int32_t V);
+bd_status launch_decode_fold(const LinearArgs& a, const LinearWorkspace& w, cudaStream_t s);
 bd_status launch_decode_tc(const LinearArgs& a, const LinearWorkspace& w, cudaStream_t s);
 bd_status launch_prefill_tc(const LinearArgs& a, const LinearWorkspace& w, cudaStream_t s);
 

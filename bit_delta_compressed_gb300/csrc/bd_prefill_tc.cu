@@ -258,11 +258,14 @@ bool prefill_tc_supported(const LinearArgs& a) {
 size_t tc_scratch_bytes(int64_t M, int64_t N, int64_t K, int32_t V) {
     size_t a = decode_tc_scratch_bytes(M, N, K, V);
     size_t b = (K % kBK == 0 && M >= 1) ? prefill_scratch_bytes(M, K) : 0;
-    return a > b ? a : b;
+    size_t c = decode_fold_scratch_bytes(M, N, K, V);
+    size_t m = a > b ? a : b;
+    return m > c ? m : c;
 }
 
 bd_path choose_path(const LinearArgs& a) {
     if (a.M <= 4) return BD_PATH_SIMT;            // GEMV: streams W_base at HBM speed
+    if (decode_fold_supported(a)) return BD_PATH_DECODE_FOLD;
     if (decode_tc_supported(a)) return BD_PATH_DECODE_TC;
     if (prefill_tc_supported(a)) return BD_PATH_PREFILL_TC;
     return BD_PATH_SIMT;

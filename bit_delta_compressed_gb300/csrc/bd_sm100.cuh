@@ -62,6 +62,37 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
     return false;
 }
 
+// try_wait that may suspend the thread for up to `ns` nanoseconds while the
+// phase is incomplete (it returns as soon as the phase completes).
+__device__ __forceinline__ bool mbar_try_wait_ns(uint64_t* bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Warp-wide bounded wait: lane 0 alone polls (suspending up to 1 us per try,
+// so waiting warps take no issue slots), the result is broadcast to the warp.
+// Gives up after `limit` tries like mbar_wait.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32_t limit, unsigned* status,
+                                          unsigned where, unsigned* diag) {
+    uint32_t ok = 1;
+    if ((threadIdx.x & 31) == 0) {
+        ok = 0;
+        for (uint32_t i = 0; i < limit && !ok; ++i) ok = mbar_try_wait_ns(bar, parity, 1000) ? 1u : 0u;
+        if (!ok) {
+            if (status) report(status, BD_ERR_TIMEOUT);
+            if (diag) atomicCAS(diag, 0u, where);
+        }
+    }
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 // ---- TMA ----------------------------------------------------------------------
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int32_t c0, int32_t c1) {

@@ -71,7 +71,10 @@ typedef enum {
     BD_PATH_AUTO = 0,
     BD_PATH_SIMT = 1,       /* CUDA-core kernel, any M */
     BD_PATH_DECODE_TC = 2,  /* tcgen05 decode kernel: base and sign products on tensor cores */
-    BD_PATH_PREFILL_TC = 3  /* tcgen05 prefill kernel: W_eff tiles built in shared memory */
+    BD_PATH_PREFILL_TC = 3, /* tcgen05 prefill kernel: W_eff tiles built in shared memory */
+    BD_PATH_DECODE_FOLD = 4 /* tcgen05 decode kernel, alpha folded into the sign operand so the
+                               base and sign products share one accumulator (M <= 128 and at
+                               most 16 distinct variants per batch) */
 } bd_path;
 
 /* ------------------------------------------------------------------ */

@@ -14,7 +14,7 @@ from tests.gpu_util import assert_y_close, bf16_np, bits_np, f32_np, load_bd
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-PATHS = ["simt", "decode_tc", "prefill_tc"]
+PATHS = ["simt", "decode_tc", "prefill_tc", "decode_fold"]
 
 
 @pytest.fixture(scope="module")
