@@ -246,8 +246,18 @@ __device__ void group_expand(const FoldParams& p, const SegPlan& pl, const FoldP
             if (ok) {
                 tc_fence_after();
                 const uint32_t col = abase + lane_addr + j * 8 * ne;
-                for (int k = 0; k < ne; ++k)
-                    store_signs(col + 8 * k, words[fp.e_slot[e0 + k] * 512 + j]);
+                int k = 0;
+                for (; k + 4 <= ne; k += 4) {           // four tiles per tensor-memory store
+                    uint32_t v[32];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t w = words[fp.e_slot[e0 + k + q] * 512 + j];
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj) v[8 * q + jj] = ((w << (7 - jj)) & 0x80808080u) ^ 0xB8B8B8B8u;
+                    }
+                    tmem_st32(col + 8 * k, v);
+                }
+                for (; k < ne; ++k) store_signs(col + 8 * k, words[fp.e_slot[e0 + k] * 512 + j]);
                 tmem_st_wait();
             }
             tc_fence_before();
@@ -450,14 +460,48 @@ __global__ void __launch_bounds__(kThreads, 1) fold_decode_kernel(const __grid_c
         if (last_cta) {
             __threadfence();
             const int rows = min(kBN, p.N - n0);
-            for (int idx = threadIdx.x; idx < p.M * rows; idx += blockDim.x) {
-                const int pos = idx / rows, rr = idx % rows;
-                float acc = 0.f;
-                for (int s = 0; s < p.splits; ++s)
-                    acc += __ldcg(p.part + (static_cast<int64_t>(s) * p.M + pos) * p.N + n0 + rr);
-                const int64_t o = static_cast<int64_t>(tok_s[pos]) * p.N + n0 + rr;
-                if (p.y_bf16) static_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(acc);
-                else static_cast<float*>(p.y)[o] = acc;
+            const int64_t sstride = static_cast<int64_t>(p.M) * p.N;        // floats per slice
+            if (rows == kBN && (p.N & 3) == 0) {
+                // four outputs per thread, slices summed in order 0, 1, 2, ...
+                // with four loads in flight
+                const int nq = kBN / 4;
+                const int64_t sq = sstride / 4;
+                for (int idx = threadIdx.x; idx < p.M * nq; idx += blockDim.x) {
+                    const int pos = idx / nq, c4 = idx % nq;
+                    const float4* src = reinterpret_cast<const float4*>(p.part + static_cast<int64_t>(pos) * p.N + n0) + c4;
+                    float4 acc = __ldcg(src);
+                    int sl = 1;
+                    for (; sl + 3 < p.splits; sl += 4) {
+                        const float4 a = __ldcg(src + sl * sq), b = __ldcg(src + (sl + 1) * sq);
+                        const float4 c = __ldcg(src + (sl + 2) * sq), d = __ldcg(src + (sl + 3) * sq);
+                        acc.x = (((acc.x + a.x) + b.x) + c.x) + d.x;
+                        acc.y = (((acc.y + a.y) + b.y) + c.y) + d.y;
+                        acc.z = (((acc.z + a.z) + b.z) + c.z) + d.z;
+                        acc.w = (((acc.w + a.w) + b.w) + c.w) + d.w;
+                    }
+                    for (; sl < p.splits; ++sl) {
+                        const float4 a = __ldcg(src + sl * sq);
+                        acc.x += a.x; acc.y += a.y; acc.z += a.z; acc.w += a.w;
+                    }
+                    const int64_t o = static_cast<int64_t>(tok_s[pos]) * p.N + n0 + 4 * c4;
+                    if (p.y_bf16) {
+                        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+                        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.y) + o) =
+                            make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+                    } else {
+                        *reinterpret_cast<float4*>(static_cast<float*>(p.y) + o) = acc;
+                    }
+                }
+            } else {
+                for (int idx = threadIdx.x; idx < p.M * rows; idx += blockDim.x) {
+                    const int pos = idx / rows, rr = idx % rows;
+                    float acc = 0.f;
+                    for (int sl = 0; sl < p.splits; ++sl)
+                        acc += __ldcg(p.part + (static_cast<int64_t>(sl) * p.M + pos) * p.N + n0 + rr);
+                    const int64_t o = static_cast<int64_t>(tok_s[pos]) * p.N + n0 + rr;
+                    if (p.y_bf16) static_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(acc);
+                    else static_cast<float*>(p.y)[o] = acc;
+                }
             }
             if (threadIdx.x == 0) p.tickets[tile] = 0u;
         }
