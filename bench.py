@@ -76,7 +76,7 @@ def peaks():
 KERNEL_SOURCES = {
     "compress_28672x8192": ["bd_compress.cu", "bd_internal.cuh"],
     "linear_stack70b": ["bd_linear.cu", "bd_paths.cuh", "bd_internal.cuh", "bd_decode_tc.cu",
-                        "bd_prefill_tc.cu", "bd_tc_common.cuh", "bd_sm100.cuh"],
+                        "bd_decode_fold.cu", "bd_prefill_tc.cu", "bd_tc_common.cuh", "bd_sm100.cuh"],
 }
 
 

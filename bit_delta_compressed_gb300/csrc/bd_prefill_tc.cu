@@ -265,7 +265,9 @@ size_t tc_scratch_bytes(int64_t M, int64_t N, int64_t K, int32_t V) {
 
 bd_path choose_path(const LinearArgs& a) {
     if (a.M <= 4) return BD_PATH_SIMT;            // GEMV: streams W_base at HBM speed
-    if (decode_fold_supported(a)) return BD_PATH_DECODE_FOLD;
+    // one variant: the per-variant sign kernel's lighter set-up wins; two or
+    // more: the folded kernel (one accumulator, issuer groups)
+    if (a.V >= 2 && decode_fold_supported(a)) return BD_PATH_DECODE_FOLD;
     if (decode_tc_supported(a)) return BD_PATH_DECODE_TC;
     if (prefill_tc_supported(a)) return BD_PATH_PREFILL_TC;
     return BD_PATH_SIMT;
