@@ -6,18 +6,20 @@
 // variant, each variant's delta arrives as packed sign bits and is expanded
 // on chip, and W_eff = W_base + alpha_v * sign(delta_v) never exists in HBM.
 //
-// The base product and the sign product accumulate into ONE tensor-memory
-// accumulator with a column per token (grouped order):
-//   D[n, t] = sum_k W[n,k] (x[t,k] 2^s_t)  +  sum_k s_v[n,k] (alpha_v x[t,k] 2^s_t)
-//   y[t, n] = 2^-s_t D[n, t]
+// Per output row n and token t (grouped order) the kernel accumulates, in
+// tensor memory,
+//   B[n, t] = sum_k W[n,k] (x[t,k] 2^s_t)             (base accumulator)
+//   S[n, t] = sum_k s_v[n,k] (alpha_v x[t,k] 2^s_t)    (sign accumulator)
+//   y[t, n] = 2^-s_t (B[n, t] + S[n, t])
 // where 2^s_t is a per-token power of two (exact) that puts the largest
 // |alpha_v x[t,k]| 2^s_t in [128, 256).  The base operand is the bf16
 // activation row scaled by 2^s_t (exact); the sign operand is alpha_v x 2^s_t
 // written as the sum of two e4m3 terms hi = rn(v), lo = rn(v - hi), which
 // keeps about 8 significant bits of every element (the same order as the
-// bf16 activations themselves).  Folding alpha into the sign operand is what
-// lets both products share one accumulator, so tensor memory holds only
-// pad16(M) accumulator columns and the rest is free for +-1 tiles.
+// bf16 activations themselves).  Folding alpha into the sign operand lets
+// every variant share ONE sign accumulator of pad16(M) columns, so tensor
+// memory holds 2 x 128 accumulator columns and the rest is free for +-1
+// tiles.
 //
 // One CTA owns 128 output rows (the 128 lanes of tensor memory) and a slice
 // of K (split-K at even 64-column blocks, summed in a fixed order by the CTA
@@ -27,19 +29,21 @@
 //     scaled activations X_c (pad16(M) rows) and the sign operand X_p (R rows)
 //     from L2; per pair of blocks one 128-row x 4-word tile of packed bits per
 //     present variant from HBM;
-//   * four issuer groups of five warps.  Group g owns the accumulator columns
-//     of a contiguous run of 16-token chunks (balanced by the grouping
-//     kernel).  Its four expansion warps (one per tensor-memory lane quarter)
-//     turn the bits of the group's entries into e4m3 +-1 tiles in tensor
-//     memory (two buffers) -- one shift and one LOP3 per four weights:
+//   * 3, the base issuer: per block four bf16 MMAs (N = pad16(M)) of the W
+//     tile with X_c; the only consumer of the W ring;
+//   * four issuer groups of five warps.  Group g owns the sign-accumulator
+//     columns of a contiguous run of 16-token chunks (balanced by the
+//     grouping kernel).  Its four expansion warps (one per tensor-memory lane
+//     quarter) turn the bits of the group's entries into e4m3 +-1 tiles in
+//     tensor memory (two buffers) -- one shift and one LOP3 per four weights:
 //     register j = ((w << (7 - j)) & 0x80808080) ^ 0xB8B8B8B8 holds columns
 //     j, j+8, j+16, j+24 of a 32-bit word -- and arrive on a named barrier;
-//     its issuer warp then issues, per 32-column K step, the bf16 base product
-//     over the group's columns and two e4m3 sign products (hi, lo) per entry
-//     (a present variant with tokens in the group's columns; variant runs that
-//     share a chunk are separated by zero rows in X_p).  Groups write
-//     disjoint columns and need no ordering among themselves; the expansion
-//     warps finally read the group's columns and write y = 2^-s_t D.
+//     its issuer warp then issues, per 32-column K step, two e4m3 sign
+//     products (hi, lo) per entry (a present variant with tokens in the
+//     group's columns; variant runs that share a chunk are separated by zero
+//     rows in X_p).  Groups write disjoint columns and need no ordering among
+//     themselves; the expansion warps finally read the group's columns of
+//     both accumulators and write y.
 // The columns inside each 32-column group of X_p are permuted to match the
 // register layout above.  MMAs are issued by converged warps (elect.sync).
 // Waiting warps poll with one lane that suspends in mbarrier.try_wait, and
@@ -61,15 +65,17 @@ constexpr int kXMax = 2;                        // activation ring stages (runti
 constexpr int kBStages = 2;                     // bits ring stages, two 64-column blocks each
 constexpr int kIss = kFoldIssuers;             // issuer groups
 constexpr int kGroupWarps = 5;                  // 4 expansion warps (one per lane quarter) + 1 issuer
-constexpr int kFirstGroup = 3;                  // warps 0, 1, 2: W, activation and bits producers
+constexpr int kBaseWarp = 3;                    // the base-product issuer
+constexpr int kFirstGroup = 4;                  // warps 0, 1, 2: W, activation and bits producers
 constexpr int kThreads = 32 * (kFirstGroup + kIss * kGroupWarps);
 constexpr int kABufs = 2;                       // +-1 tile buffers per group
-constexpr int kACol0 = kFoldMaxCols;            // +-1 tiles after the accumulator
-constexpr int kAEntries = (512 - kFoldMaxCols) / (8 * kABufs);   // entries whose tiles fit
+constexpr int kSCol0 = kFoldMaxCols;            // sign accumulator after the base accumulator
+constexpr int kACol0 = 2 * kFoldMaxCols;        // +-1 tiles after both accumulators
+constexpr int kAEntries = (512 - kACol0) / (8 * kABufs);   // entries whose tiles fit
 constexpr int kTmemCols = 512;
 constexpr uint32_t kWaitLimit = 1u << 20;
 constexpr uint32_t kWTile = kBN * 128;
-static_assert(kAEntries >= kFoldMaxEntries, "tensor memory budget");
+static_assert(kAEntries >= kFoldSepEntries, "tensor memory budget");
 
 struct FoldParams {
     CUtensorMap tm_w;                           // W_base [N, K] bf16, box 128 rows
@@ -143,43 +149,62 @@ constexpr unsigned kFull = 0xffffffffu;
 // Named barrier of group g's +-1 tile buffer b (barrier 0 is __syncthreads).
 __device__ __forceinline__ int group_bar(int g, int b) { return 1 + kABufs * g + b; }
 
-// The issuer warp of a group: per 32-column K step j of block i, wait for the
-// group's tiles (named barrier), then issue the base product over the
-// group's columns and the hi/lo sign products of its entries.  Every barrier
-// is visited on every step, also after an error, so the group never blocks.
-__device__ void group_issue(const FoldParams& p, const FoldPlan& fp, uint32_t tmem, uint32_t abase, int bcol,
-                            int bn, int e0, int ne, int g, int nkb, uint8_t* wring, uint8_t* xring,
-                            uint32_t xs_bytes, uint64_t* w_full, uint64_t* w_empty, uint64_t* x_full,
+// The base issuer: per 64-column block, the bf16 product of the W tile with
+// all pad16(M) scaled activation rows into the base accumulator (one MMA per
+// 16 columns of K, N = pad16(M)), then release the W and activation stages.
+__device__ void base_issue(const FoldParams& p, uint32_t tmem, int nkb, uint8_t* wring, uint8_t* xring,
+                           uint32_t xs_bytes, uint64_t* w_full, uint64_t* w_empty, uint64_t* x_full,
+                           uint64_t* x_empty, uint64_t* acc_full, uint64_t* drain) {
+    using namespace sm100;
+    const uint32_t idb = idesc_bf16(128, p.Mb);
+    bool ok = true;
+    for (int i = 0; i < nkb && ok; ++i) {
+        const int ws = i % p.wstages, xs = i % p.xstages;
+        ok = warp_wait(&x_full[xs], (i / p.xstages) & 1, kWaitLimit, p.status, 26, p.diag);
+        if (ok) ok = warp_wait(&w_full[ws], (i / p.wstages) & 1, kWaitLimit, p.status, 27, p.diag);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t sw = smem_u32(wring + ws * kWTile);
+        const uint32_t sx = smem_u32(xring + xs * xs_bytes);
+#pragma unroll
+        for (int k16 = 0; k16 < 4; ++k16)
+            mma_bf16_ss(tmem, desc_sw128(sw + 32 * k16), desc_sw128(sx + 32 * k16), idb,
+                        (i > 0 || k16 > 0) ? 1u : 0u);
+        commit_elect(&w_empty[ws]);
+        commit_elect(&x_empty[xs]);
+    }
+    __syncwarp();
+    if (ok) commit_elect(acc_full);
+    commit_elect(drain);                     // completes when every MMA of this warp has
+}
+
+// The sign issuer warp of a group: per 32-column K step j of block i, wait
+// for the group's tiles (named barrier), then issue the hi/lo sign products
+// of its entries into the sign accumulator (zeroed by the expansion warps
+// before the first step).  Every barrier is visited on every step, also
+// after an error, so the group never blocks.
+__device__ void group_issue(const FoldParams& p, const FoldPlan& fp, uint32_t tmem, uint32_t abase, int e0,
+                            int ne, int g, int nkb, uint8_t* xring, uint32_t xs_bytes, uint64_t* x_full,
                             uint64_t* x_empty, uint64_t* ge, uint64_t* acc_full, uint64_t* drain) {
     using namespace sm100;
     const int lane = threadIdx.x & 31;
-    const bool work = bn > 0;
-    const uint32_t idb = idesc_bf16(128, work ? bn : 16);
+    const bool work = ne > 0;
     const int Mb = p.Mb;
     bool ok = true;
     for (int i = 0; i < nkb; ++i) {
-        const int ws = i % p.wstages, xs = i % p.xstages;
+        const int xs = i % p.xstages;
         for (int j = 0; j < 2; ++j) {
             named_sync(group_bar(g, j), kGroupThreads);
-            if (ok && j == 0) {
-                ok = warp_wait(&x_full[xs], (i / p.xstages) & 1, kWaitLimit, p.status, 26, p.diag);
-                if (ok) ok = warp_wait(&w_full[ws], (i / p.wstages) & 1, kWaitLimit, p.status, 27, p.diag);
-            }
+            // every group, also one without entries, waits for the stage it
+            // releases: an early arrival would count towards a later phase
+            if (ok && j == 0) ok = warp_wait(&x_full[xs], (i / p.xstages) & 1, kWaitLimit, p.status, 26, p.diag);
             if (!ok) continue;
-            tc_fence_after();
             if (work) {
-                const uint32_t sw = smem_u32(wring + ws * kWTile);
-                const uint32_t sx = smem_u32(xring + xs * xs_bytes);
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int k16 = 2 * j + h;
-                    mma_bf16_ss(tmem + bcol, desc_sw128(sw + 32 * k16), desc_sw128(sx + bcol * 128 + 32 * k16), idb,
-                                (i > 0 || k16 > 0) ? 1u : 0u);
-                }
-                const uint32_t sxp = sx + Mb * 128;
+                tc_fence_after();
+                const uint32_t sxp = smem_u32(xring + xs * xs_bytes) + Mb * 128;
                 const uint32_t abuf = abase + j * 8 * ne;
                 for (int e = e0; e < e0 + ne; ++e) {
-                    const uint32_t d = tmem + fp.e_col[e];
+                    const uint32_t d = tmem + kSCol0 + fp.e_col[e];
                     const uint32_t a = abuf + 8 * (e - e0);
                     const uint32_t brow = sxp + fp.e_row[e] * 128 + 32 * j;
                     const uint32_t id8 = idesc_e4m3(128, fp.e_n[e]);
@@ -187,15 +212,12 @@ __device__ void group_issue(const FoldParams& p, const FoldPlan& fp, uint32_t tm
                     mma_e4m3_ts(d, a, desc_sw128(brow + 64), id8);
                 }
                 commit_elect(&ge[j]);
-                if (j == 1) {
-                    commit_elect(&x_empty[xs]);
-                    commit_elect(&w_empty[ws]);
-                }
+                if (j == 1) commit_elect(&x_empty[xs]);
             } else {
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&ge[j]);
-                    if (j == 1) { mbar_arrive(&x_empty[xs]); mbar_arrive(&w_empty[ws]); }
+                    if (j == 1) mbar_arrive(&x_empty[xs]);
                 }
             }
         }
@@ -203,7 +225,7 @@ __device__ void group_issue(const FoldParams& p, const FoldPlan& fp, uint32_t tm
     __syncwarp();
     if (work) {
         if (ok) commit_elect(acc_full);
-        commit_elect(drain);                 // completes when every MMA of this warp has
+        commit_elect(drain);
     } else if (lane == 0) {
         if (ok) mbar_arrive(acc_full);
         mbar_arrive(drain);
@@ -236,6 +258,14 @@ __device__ void group_expand(const FoldParams& p, const SegPlan& pl, const FoldP
     const int n = n0 + r;
     const bool row_ok = n < p.N;
     const uint32_t lane_addr = static_cast<uint32_t>(32 * q4) << 16;
+    {
+        // the sign products all accumulate: start the group's columns at zero
+        uint32_t z[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) z[jj] = 0u;
+        for (int c = bcol; c < bcol + bn; c += 8) tmem_st8(tmem + lane_addr + kSCol0 + c, z);
+        tmem_st_wait();
+    }
     bool ok = true;
     for (int i = 0; i < nkb; ++i) {
         const int m = i >> 1, half = i & 1, bs = m & 1;
@@ -268,21 +298,23 @@ __device__ void group_expand(const FoldParams& p, const SegPlan& pl, const FoldP
             if (lane == 0) mbar_arrive(&b_empty[bs]);
         }
     }
-    // ---- epilogue: y = 2^-s_t D over the group's columns ----
+    // ---- epilogue: y = 2^-s_t (D_base + D_sign) over the group's columns ----
     if (ok) ok = warp_wait(acc_full, 0, kWaitLimit, p.status, 29, p.diag);
     if (!ok) return;
     tc_fence_after();
     const int n_valid = pl.M - pl.n_invalid;
     for (int c0 = bcol; c0 < bcol + bn; c0 += 16) {
-        uint32_t v[16];
+        uint32_t v[16], u[16];
         tmem_ld16(tmem + lane_addr + c0, v);
+        tmem_ld16(tmem + lane_addr + kSCol0 + c0, u);
         tmem_ld_wait();
         if (row_ok) {
 #pragma unroll
             for (int t = 0; t < 16; ++t) {
                 const int pos = c0 + t;
                 if (pos >= p.M) break;
-                const float val = pos < n_valid ? __uint_as_float(v[t]) * scale_s[pos] : 0.f;
+                const float d = __uint_as_float(v[t]) + __uint_as_float(u[t]);
+                const float val = pos < n_valid ? d * scale_s[pos] : 0.f;
                 store_out(p, split, pos, tok_s[pos], n, val);
             }
         }
@@ -321,13 +353,13 @@ __global__ void __launch_bounds__(kThreads, 1) fold_decode_kernel(const __grid_c
     const int nkb = kb1 - kb0;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kWMax; ++s) { mbar_init(&w_full[s], 1); mbar_init(&w_empty[s], kIss); }
-        for (int s = 0; s < kXMax; ++s) { mbar_init(&x_full[s], 1); mbar_init(&x_empty[s], kIss); }
+        for (int s = 0; s < kWMax; ++s) { mbar_init(&w_full[s], 1); mbar_init(&w_empty[s], 1); }
+        for (int s = 0; s < kXMax; ++s) { mbar_init(&x_full[s], 1); mbar_init(&x_empty[s], kIss + 1); }
         for (int s = 0; s < kBStages; ++s) { mbar_init(&b_full[s], 1); mbar_init(&b_empty[s], 4 * kIss); }
         for (int g = 0; g < kIss; ++g)
             for (int b = 0; b < kABufs; ++b) mbar_init(&g_empty[g][b], 1);
-        mbar_init(&acc_full, kIss);
-        mbar_init(&drain, kIss);
+        mbar_init(&acc_full, kIss + 1);
+        mbar_init(&drain, kIss + 1);
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(&tmem_base, kTmemCols);
@@ -426,6 +458,8 @@ __global__ void __launch_bounds__(kThreads, 1) fold_decode_kernel(const __grid_c
                 mbar_wait(&b_full[s], (last / kBStages) & 1, kWaitLimit, p.status, 33, p.diag);
             }
         }
+    } else if (warp == kBaseWarp) {
+        base_issue(p, tmem, nkb, wring, xring, xs_bytes, w_full, w_empty, x_full, x_empty, &acc_full, &drain);
     } else {
         // ---------------- issuer groups ----------------
         // Group g: four expansion warps (one per tensor-memory lane quarter)
@@ -441,8 +475,8 @@ __global__ void __launch_bounds__(kThreads, 1) fold_decode_kernel(const __grid_c
         for (int h = 0; h < g; ++h) a0 += 8 * kABufs * fp.iss_ne[h];
         const uint32_t abase = tmem + kACol0 + a0;
         if (gw == kGroupWarps - 1)
-            group_issue(p, fp, tmem, abase, bcol, bn, e0, ne, g, nkb, wring, xring, xs_bytes, w_full, w_empty,
-                        x_full, x_empty, g_empty[g], &acc_full, &drain);
+            group_issue(p, fp, tmem, abase, e0, ne, g, nkb, xring, xs_bytes, x_full, x_empty, g_empty[g], &acc_full,
+                        &drain);
         else
             group_expand(p, pl, fp, tmem, abase, e0, ne, g, warp % 4, n0, nkb, g_empty[g], bring, bstage_bytes,
                          b_full, b_empty, &acc_full, tok_s, scale_s, split, bcol, bn);
@@ -680,7 +714,7 @@ int fold_rmax(int64_t M, int32_t V) {
 int fold_splits(int64_t n_tiles, int kb_total, int sms, int dmax, int64_t M) {
     const double hbm_us = (16.0 + dmax) * 1024.0 / 45.0e3;
     const int entries = (dmax + kIss - 1) / kIss + 1;
-    const double issue_us = 2.0 * (2 + 2 * entries) * 55.0 / 2000.0;
+    const double issue_us = 2.0 * (2 * entries) * 55.0 / 2000.0;
     const double kb_us = hbm_us > issue_us ? hbm_us : issue_us;
     const double fixed_us = 4.0;
     const double reduce_us_per_split = static_cast<double>(M) * kBN * 4.0 / 100.0e3;

@@ -78,11 +78,13 @@ struct SegPlan {
 // product over its range plus one "entry" per present variant whose tokens
 // fall inside it.  Entry e covers columns [e_col, e_col + e_n) with rows
 // [e_row, e_row + e_n) of the sign operand (rows of other variants' tokens
-// are zero there) and the +-1 tile of present variant e_slot.
+// are zero there) and the +-1 tile of present variant e_slot.  The base
+// product (all columns at once) has an issuer of its own.
 constexpr int kFoldIssuers = 4;
 constexpr int kFoldMaxSlots = 16;                       // present variants
 constexpr int kFoldMaxEntries = kFoldMaxSlots + kFoldIssuers;
 constexpr int kFoldMaxCols = 128;                       // pad16(M)
+constexpr int kFoldSepEntries = 16;                     // entries whose +-1 tiles fit (two buffers)
 struct FoldPlan {
     int32_t ok;                                   // 1 if the batch fits the folded kernel
     int32_t C;                                    // chunks of 16 columns

@@ -57,10 +57,12 @@ __device__ __forceinline__ int bucket_of(int32_t id, int V) {
 }
 
 // Issue plan of the folded decode kernel (one thread).  The 16-column chunks
-// of the accumulator are cut into kFoldIssuers contiguous ranges so that the
-// largest per-range MMA count per K step -- 2 base products plus 2 (hi, lo)
-// per variant touching the range -- is as small as possible (a tiny dynamic
-// programme over at most 8 chunks).
+// of the sign accumulator are cut into at most kFoldIssuers contiguous ranges
+// so that the largest per-range sign-MMA count per K step -- 2 (hi, lo) per
+// variant touching the range -- is as small as possible (a tiny dynamic
+// programme over at most 8 chunks).  A variant cut by a range boundary costs
+// an extra entry; when the entries would not fit the kernel's +-1 tile
+// buffers (kFoldSepEntries), fewer ranges are used (one range always fits).
 __device__ void fold_plan(const SegPlan& pl, int M, FoldPlan* fp) {
     constexpr int I = kFoldIssuers;
     constexpr int CM = kFoldMaxCols / 16;
@@ -81,24 +83,30 @@ __device__ void fold_plan(const SegPlan& pl, int M, FoldPlan* fp) {
         if (b <= a) return 0;
         uint32_t m = 0;
         for (int c = a; c < b; ++c) m |= mask[c];
-        return 2 + 2 * __popc(m);
+        return 2 * __popc(m);
     };
     constexpr int kBig = 1 << 20;
-    int f[I + 1][CM + 1], arg[I + 1][CM + 1];
-    for (int c = 0; c <= C; ++c) { f[0][c] = c == 0 ? 0 : kBig; arg[0][c] = 0; }
-    for (int i = 1; i <= I; ++i)
-        for (int c = 0; c <= C; ++c) {
-            int best = kBig, ba = 0;
-            for (int a = 0; a <= c; ++a) {
-                const int v = max(f[i - 1][a], cost(a, c));
-                if (v < best) { best = v; ba = a; }
-            }
-            f[i][c] = best;
-            arg[i][c] = ba;
-        }
     int bnd[I + 1];
-    bnd[I] = C;
-    for (int i = I; i >= 1; --i) bnd[i - 1] = arg[i][bnd[i]];
+    for (int G = I; G >= 1; --G) {
+        int f[I + 1][CM + 1], arg[I + 1][CM + 1];
+        for (int c = 0; c <= C; ++c) { f[0][c] = c == 0 ? 0 : kBig; arg[0][c] = 0; }
+        for (int i = 1; i <= G; ++i)
+            for (int c = 0; c <= C; ++c) {
+                int best = kBig, ba = 0;
+                for (int a = 0; a <= c; ++a) {
+                    const int v = max(f[i - 1][a], cost(a, c));
+                    if (v < best) { best = v; ba = a; }
+                }
+                f[i][c] = best;
+                arg[i][c] = ba;
+            }
+        for (int i = G + 1; i <= I; ++i) bnd[i] = C;
+        bnd[G] = C;
+        for (int i = G; i >= 1; --i) bnd[i - 1] = arg[i][bnd[i]];
+        int entries = 0;
+        for (int i = 0; i < G; ++i) entries += cost(bnd[i], bnd[i + 1]) / 2;
+        if (entries <= kFoldSepEntries) break;
+    }
     int e = 0, row = 0;
     for (int i = 0; i < I; ++i) {
         const int a = bnd[i], b = bnd[i + 1];
