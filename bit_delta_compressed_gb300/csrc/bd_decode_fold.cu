@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1) fold_decode_kernel(const __grid_c
             int issued = 0;
             for (int i = 0; i < nkb; ++i) {
                 const int ws = i % p.wstages;
-                if (!mbar_wait(&w_empty[ws], ((i / p.wstages) & 1) ^ 1, kWaitLimit, p.status, 21, p.diag)) break;
+                if (!mbar_wait_sleep(&w_empty[ws], ((i / p.wstages) & 1) ^ 1, kWaitLimit, p.status, 21, p.diag)) break;
                 mbar_expect_tx(&w_full[ws], kWTile);
                 tma_load_2d(wring + ws * kWTile, &p.tm_w, &w_full[ws], (kb0 + i) * kBK, n0);
                 issued = i + 1;
@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1) fold_decode_kernel(const __grid_c
             // still writing shared memory when the CTA exits
             for (int s = 0; s < p.wstages && s < issued; ++s) {
                 const int last = issued - 1 - ((issued - 1 - s) % p.wstages);
-                mbar_wait(&w_full[s], (last / p.wstages) & 1, kWaitLimit, p.status, 23, p.diag);
+                mbar_wait_sleep(&w_full[s], (last / p.wstages) & 1, kWaitLimit, p.status, 23, p.diag);
             }
         }
     } else if (warp == 1) {
@@ -420,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1) fold_decode_kernel(const __grid_c
             for (int i = 0; i < nkb; ++i) {
                 const int kb = kb0 + i;
                 const int xs = i % p.xstages;
-                if (!mbar_wait(&x_empty[xs], ((i / p.xstages) & 1) ^ 1, kWaitLimit, p.status, 22, p.diag)) break;
+                if (!mbar_wait_sleep(&x_empty[xs], ((i / p.xstages) & 1) ^ 1, kWaitLimit, p.status, 22, p.diag)) break;
                 uint8_t* sx = xring + xs * xs_bytes;
                 mbar_expect_tx(&x_full[xs], static_cast<uint32_t>(Mb + R) * 128u);
                 tma_load_2d(sx, &p.tm_xc, &x_full[xs], kb * kBK, 0);
@@ -432,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1) fold_decode_kernel(const __grid_c
             }
             for (int s = 0; s < p.xstages && s < issued; ++s) {
                 const int last = issued - 1 - ((issued - 1 - s) % p.xstages);
-                mbar_wait(&x_full[s], (last / p.xstages) & 1, kWaitLimit, p.status, 24, p.diag);
+                mbar_wait_sleep(&x_full[s], (last / p.xstages) & 1, kWaitLimit, p.status, 24, p.diag);
             }
         }
     } else if (warp == 2) {
@@ -445,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1) fold_decode_kernel(const __grid_c
             int issued = 0;
             for (int m = 0; m < np; ++m) {
                 const int bs = m % kBStages;
-                if (!mbar_wait(&b_empty[bs], ((m / kBStages) & 1) ^ 1, kWaitLimit, p.status, 32, p.diag)) break;
+                if (!mbar_wait_sleep(&b_empty[bs], ((m / kBStages) & 1) ^ 1, kWaitLimit, p.status, 32, p.diag)) break;
                 if (D == 0) { mbar_arrive(&b_full[bs]); issued = m + 1; continue; }
                 mbar_expect_tx(&b_full[bs], static_cast<uint32_t>(D) * 2048u);
                 uint8_t* sb = bring + bs * bstage_bytes;
@@ -455,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1) fold_decode_kernel(const __grid_c
             }
             for (int s = 0; s < kBStages && s < issued; ++s) {
                 const int last = issued - 1 - ((issued - 1 - s) % kBStages);
-                mbar_wait(&b_full[s], (last / kBStages) & 1, kWaitLimit, p.status, 33, p.diag);
+                mbar_wait_sleep(&b_full[s], (last / kBStages) & 1, kWaitLimit, p.status, 33, p.diag);
             }
         }
     } else if (warp == kBaseWarp) {
@@ -542,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1) fold_decode_kernel(const __grid_c
     }
     if (warp == 0) {
         // every MMA this CTA issued has completed before its tensor memory is freed
-        if (plan_ok) mbar_wait(&drain, 0, kWaitLimit, p.status, 30, p.diag);
+        if (plan_ok) mbar_wait_sleep(&drain, 0, kWaitLimit, p.status, 30, p.diag);
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }

@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                     if (kb == kb0 || (kb & 1) == 0) {
                         // bits of every variant of the pass for the K-block pair kb & ~1
                         const int b = bt % kBitStages;
-                        if (!(ok = mbar_wait(&bits_empty[b], ((bt / kBitStages) & 1) ^ 1, kWaitLimit, p.status, 8, p.diag))) break;
+                        if (!(ok = mbar_wait_sleep(&bits_empty[b], ((bt / kBitStages) & 1) ^ 1, kWaitLimit, p.status, 8, p.diag))) break;
                         mbar_expect_tx(&bits_full[b], (q.d1 - q.d0) * kBitsTile);
                         uint8_t* sb = base + L.bits + b * L.bits_stage;
                         for (int d = q.d0; d < q.d1; ++d)
@@ -225,13 +225,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                     }
                     if (g == 0) {
                         const int s = wt % kWStages;
-                        if (!(ok = mbar_wait(&w_empty[s], ((wt / kWStages) & 1) ^ 1, kWaitLimit, p.status, 1, p.diag))) break;
+                        if (!(ok = mbar_wait_sleep(&w_empty[s], ((wt / kWStages) & 1) ^ 1, kWaitLimit, p.status, 1, p.diag))) break;
                         mbar_expect_tx(&w_full[s], kWTile);
                         tma_load_2d(base + L.w + s * kWTile, &p.tm_w, &w_full[s], kb * kBK, n0);
                         ++wt;
                     }
                     const int s = xt % kXStages;
-                    if (!(ok = mbar_wait(&x_empty[s], ((xt / kXStages) & 1) ^ 1, kWaitLimit, p.status, 10, p.diag))) break;
+                    if (!(ok = mbar_wait_sleep(&x_empty[s], ((xt / kXStages) & 1) ^ 1, kWaitLimit, p.status, 10, p.diag))) break;
                     mbar_expect_tx(&x_full[s], q.rows * 128 + (g == 0 ? Mb * 128 : 0));
                     uint8_t* sx = base + L.x + s * L.x_stage;
                     if (g == 0) tma_load_2d(sx, &p.tm_xc, &x_full[s], kb * kBK, 0);
@@ -254,10 +254,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             for (int g = 0; g < n_groups && ok; ++g) {
                 for (int i = 0; i < nkb && ok; ++i, ++xt) {
                     const int s = xt % kXStages;
-                    if (!(ok = mbar_wait(&x_full[s], (xt / kXStages) & 1, kWaitLimit, p.status, 2, p.diag))) break;
+                    if (!(ok = mbar_wait_sleep(&x_full[s], (xt / kXStages) & 1, kWaitLimit, p.status, 2, p.diag))) break;
                     if (g == 0) {
                         const int ws = i % kWStages;
-                        if (!(ok = mbar_wait(&w_full[ws], (i / kWStages) & 1, kWaitLimit, p.status, 11, p.diag))) break;
+                        if (!(ok = mbar_wait_sleep(&w_full[ws], (i / kWStages) & 1, kWaitLimit, p.status, 11, p.diag))) break;
                         tc_fence_after();
                         const uint32_t sw = smem_u32(base + L.w + ws * kWTile);
                         const uint32_t sxc = smem_u32(base + L.x + s * L.x_stage);
@@ -281,10 +281,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             for (int g = 0; g < n_groups && ok; ++g) {
                 const PassInfo q = pass_info(pl, g);
                 const int nd = q.d1 - q.d0;
-                if (g > 0 && !(ok = mbar_wait(&acc_empty, (g - 1) & 1, kWaitLimit, p.status, 3, p.diag))) break;
+                if (g > 0 && !(ok = mbar_wait_sleep(&acc_empty, (g - 1) & 1, kWaitLimit, p.status, 3, p.diag))) break;
                 for (int i = 0; i < nkb && ok; ++i, ++it) {
                     const int s = it % kXStages;
-                    if (!(ok = mbar_wait(&x_full[s], (it / kXStages) & 1, kWaitLimit, p.status, 4, p.diag))) break;
+                    if (!(ok = mbar_wait_sleep(&x_full[s], (it / kXStages) & 1, kWaitLimit, p.status, 4, p.diag))) break;
                     const uint32_t sxp = smem_u32(base + L.x + s * L.x_stage + L.xp_off);
                     for (int dl = me; dl < nd && ok; dl += kIssuers) {
                         const int d = q.d0 + dl;
@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                         const uint32_t dcol = kBaseCol + Mb + segr;
                         const uint32_t idesc = idesc_e4m3(128, pad16(pl.cnt[d]));
                         for (int h = 0; h < 2 && ok; ++h, ++u) {
-                            if (!(ok = mbar_wait(&tm_full[me][h], (u >> 1) & 1, kWaitLimit, p.status, 5, p.diag))) break;
+                            if (!(ok = mbar_wait_sleep(&tm_full[me][h], (u >> 1) & 1, kWaitLimit, p.status, 5, p.diag))) break;
                             tc_fence_after();
                             const uint32_t a = tmem + me * 2 * kSlotCols + h * kSlotCols;
                             const uint32_t brow = sxp + segr * 128 + 32 * h;
@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                 const int kb = kb0 + i;
                 const int b = bt % kBitStages;
                 if (i == 0 || (kb & 1) == 0) {
-                    if (!(ok = mbar_wait(&bits_full[b], (bt / kBitStages) & 1, kWaitLimit, p.status, 9, p.diag))) break;
+                    if (!(ok = mbar_wait_sleep(&bits_full[b], (bt / kBitStages) & 1, kWaitLimit, p.status, 9, p.diag))) break;
                 }
                 const uint32_t* sb = reinterpret_cast<const uint32_t*>(base + L.bits + b * L.bits_stage) +
                                      r * 4 + 2 * (kb & 1) + h;
@@ -335,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                     const int iss = dl % kIssuers;
                     const uint32_t u = ubase[iss] + 2 * (i * issuer_count(nd, iss) + dl / kIssuers) + h;
                     const uint32_t w = sb[dl * (kBitsTile / 4)];
-                    if (!(ok = mbar_wait(&tm_empty[iss][h], ((u >> 1) & 1) ^ 1, kWaitLimit, p.status, 6, p.diag))) break;
+                    if (!(ok = mbar_wait_sleep(&tm_empty[iss][h], ((u >> 1) & 1) ^ 1, kWaitLimit, p.status, 6, p.diag))) break;
                     tc_fence_after();
                     uint32_t v[8];
 #pragma unroll
@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             for (int i = 0; i < kIssuers; ++i) ubase[i] += 2 * nkb * issuer_count(nd, i);
             if (!ok) break;
             // ---- epilogue of pass g ----
-            if (!(ok = mbar_wait(&acc_full, g & 1, kWaitLimit, p.status, 7, p.diag))) break;
+            if (!(ok = mbar_wait_sleep(&acc_full, g & 1, kWaitLimit, p.status, 7, p.diag))) break;
             tc_fence_after();
             if (g == 0) {
                 for (int pos0 = 8 * h; pos0 < pl.n_base; pos0 += 16) {     // base-model tokens

@@ -96,7 +96,7 @@ struct FoldPlan {
 
 struct GroupView {
     int32_t* counts;     // [V + 2]: bucket 0 = id -1 (base), 1..V = variants, V+1 = invalid
-    int32_t* offsets;    // [V + 3]: exclusive prefix of counts
+    int32_t* offsets;    // [V + 3]: first grouped position of each bucket; [V + 2] = M
     int32_t* pos2tok;    // [M]: grouped position -> original token
     int32_t* pos_var;    // [M]: grouped position -> variant id (-1 base, -2 invalid)
     SegPlan* plan;

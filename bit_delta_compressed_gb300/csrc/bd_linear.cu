@@ -56,37 +56,38 @@ __device__ __forceinline__ int bucket_of(int32_t id, int V) {
     return (id >= -1 && id < V) ? id + 1 : V + 1;
 }
 
-// Issue plan of the folded decode kernel (one thread).  The 16-column chunks
-// of the sign accumulator are cut into at most kFoldIssuers contiguous ranges
-// so that the largest per-range sign-MMA count per K step -- 2 (hi, lo) per
-// variant touching the range -- is as small as possible (a tiny dynamic
-// programme over at most 8 chunks).  A variant cut by a range boundary costs
-// an extra entry; when the entries would not fit the kernel's +-1 tile
-// buffers (kFoldSepEntries), fewer ranges are used (one range always fits).
-__device__ void fold_plan(const SegPlan& pl, int M, FoldPlan* fp) {
-    constexpr int I = kFoldIssuers;
-    constexpr int CM = kFoldMaxCols / 16;
-    const int C = pad16(M) / 16;
-    fp->ok = 0;
-    fp->C = C;
-    fp->R = 0;
-    fp->n_entries = 0;
-    for (int i = 0; i < I; ++i) { fp->iss_col[i] = 0; fp->iss_n[i] = 0; fp->iss_e0[i] = 0; fp->iss_ne[i] = 0; }
-    if (C > CM || pl.D > kFoldMaxSlots) return;
-    uint32_t mask[CM];
-    for (int c = 0; c < CM; ++c) mask[c] = 0;
-    for (int d = 0; d < pl.D; ++d) {
-        const int c0 = pl.off[d] / 16, c1 = (pl.off[d] + pl.cnt[d] - 1) / 16;
+// Issue plan of the folded decode kernel.  The 16-column chunks of the sign
+// accumulator are cut into at most kFoldIssuers contiguous ranges so that
+// the largest per-range entry count -- one entry (two sign MMAs, hi and lo,
+// per K step) per variant run touching the range -- is as small as possible
+// (a tiny dynamic programme over at most 8 chunks).  A run cut by a range
+// boundary costs an extra entry; when the entries would not fit the
+// kernel's +-1 tile buffers (kFoldSepEntries), fewer ranges are used (one
+// range always fits).
+constexpr int kFoldChunks = kFoldMaxCols / 16;
+
+// Bit d of mask[c]: run d (first position off[d], cnt[d] tokens) has a token
+// in chunk c.
+__device__ void fold_masks(const int32_t* off, const int32_t* cnt, int D, uint32_t* mask) {
+    for (int c = 0; c < kFoldChunks; ++c) mask[c] = 0;
+    for (int d = 0; d < D; ++d) {
+        const int c0 = off[d] / 16, c1 = (off[d] + cnt[d] - 1) / 16;
         for (int c = c0; c <= c1; ++c) mask[c] |= 1u << d;
     }
-    auto cost = [&](int a, int b) {
-        if (b <= a) return 0;
+}
+
+// Range boundaries bnd[0..kFoldIssuers] over C chunks; returns the busiest
+// range's entry count.
+__device__ int fold_ranges(const uint32_t* mask, int C, int* bnd) {
+    constexpr int I = kFoldIssuers, CM = kFoldChunks;
+    int cst[CM + 1][CM + 1];                      // entries of chunk range [a, b)
+    for (int a = 0; a <= C; ++a) {
         uint32_t m = 0;
-        for (int c = a; c < b; ++c) m |= mask[c];
-        return 2 * __popc(m);
-    };
+        cst[a][a] = 0;
+        for (int b = a + 1; b <= C; ++b) { m |= mask[b - 1]; cst[a][b] = __popc(m); }
+    }
     constexpr int kBig = 1 << 20;
-    int bnd[I + 1];
+    int worst = 0;
     for (int G = I; G >= 1; --G) {
         int f[I + 1][CM + 1], arg[I + 1][CM + 1];
         for (int c = 0; c <= C; ++c) { f[0][c] = c == 0 ? 0 : kBig; arg[0][c] = 0; }
@@ -94,7 +95,7 @@ __device__ void fold_plan(const SegPlan& pl, int M, FoldPlan* fp) {
             for (int c = 0; c <= C; ++c) {
                 int best = kBig, ba = 0;
                 for (int a = 0; a <= c; ++a) {
-                    const int v = max(f[i - 1][a], cost(a, c));
+                    const int v = max(f[i - 1][a], cst[a][c]);
                     if (v < best) { best = v; ba = a; }
                 }
                 f[i][c] = best;
@@ -104,9 +105,29 @@ __device__ void fold_plan(const SegPlan& pl, int M, FoldPlan* fp) {
         bnd[G] = C;
         for (int i = G; i >= 1; --i) bnd[i - 1] = arg[i][bnd[i]];
         int entries = 0;
-        for (int i = 0; i < G; ++i) entries += cost(bnd[i], bnd[i + 1]) / 2;
+        worst = 0;
+        for (int i = 0; i < G; ++i) {
+            entries += cst[bnd[i]][bnd[i + 1]];
+            worst = max(worst, cst[bnd[i]][bnd[i + 1]]);
+        }
         if (entries <= kFoldSepEntries) break;
     }
+    return worst;
+}
+
+__device__ void fold_plan(const SegPlan& pl, int M, FoldPlan* fp) {
+    constexpr int I = kFoldIssuers;
+    const int C = pad16(M) / 16;
+    fp->ok = 0;
+    fp->C = C;
+    fp->R = 0;
+    fp->n_entries = 0;
+    for (int i = 0; i < I; ++i) { fp->iss_col[i] = 0; fp->iss_n[i] = 0; fp->iss_e0[i] = 0; fp->iss_ne[i] = 0; }
+    if (C > kFoldChunks || pl.D > kFoldMaxSlots) return;
+    uint32_t mask[kFoldChunks];
+    fold_masks(pl.off, pl.cnt, pl.D, mask);
+    int bnd[I + 1];
+    fold_ranges(mask, C, bnd);
     int e = 0, row = 0;
     for (int i = 0; i < I; ++i) {
         const int a = bnd[i], b = bnd[i + 1];
@@ -131,6 +152,49 @@ __device__ void fold_plan(const SegPlan& pl, int M, FoldPlan* fp) {
     fp->ok = 1;
 }
 
+// Order of the variant runs in the grouped layout.  Candidate 0 is the id
+// order; candidate c > 0 is a seeded shuffle of it (Fisher-Yates, indices
+// drawn with the "lowbias32" integer hash of c and the step).
+constexpr int kOrderTries = 1;                   // candidates per thread
+__device__ __forceinline__ uint32_t lowbias32(uint32_t x) {
+    x ^= x >> 16;
+    x *= 0x7feb352du;
+    x ^= x >> 15;
+    x *= 0x846ca68bu;
+    x ^= x >> 16;
+    return x;
+}
+__device__ void run_order(int cand, const int* present, int D, int* ord) {
+    for (int d = 0; d < D; ++d) ord[d] = present[d];
+    if (cand == 0) return;
+    for (int i = D - 1; i > 0; --i) {
+        const int j = static_cast<int>(lowbias32(static_cast<uint32_t>(cand) * 0x9E3779B9u + static_cast<uint32_t>(i)) %
+                                       static_cast<uint32_t>(i + 1));
+        const int t = ord[i];
+        ord[i] = ord[j];
+        ord[j] = t;
+    }
+}
+
+// Score of an order for the folded kernel: busiest issuer's entries first,
+// then the sign-operand rows (in chunks).
+__device__ int order_score(const int* ord, int D, const int* total, int n_base, int C) {
+    int32_t off[kFoldMaxSlots], cnt[kFoldMaxSlots];
+    int run = n_base;
+    for (int d = 0; d < D; ++d) {
+        off[d] = run;
+        cnt[d] = total[ord[d] + 1];
+        run += cnt[d];
+    }
+    uint32_t mask[kFoldChunks];
+    fold_masks(off, cnt, D, mask);
+    int bnd[kFoldIssuers + 1];
+    const int worst = fold_ranges(mask, C, bnd);
+    int rows = 0;
+    for (int c = 0; c < C; ++c) rows += __popc(mask[c]);
+    return worst * 256 + rows;
+}
+
 __global__ void __launch_bounds__(1024) group_kernel(const int32_t* __restrict__ ids, int M, int V,
                                                      int group_budget, GroupView g,
                                                      unsigned* status) {
@@ -150,25 +214,78 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t* __restrict__
         atomicAdd(&total[b], 1);
     }
     if (__syncthreads_or(bad) && threadIdx.x == 0) report(status, BD_ERR_VARIANT);
-    if (threadIdx.x == 0) {
-        int run = 0;
-        for (int b = 0; b < nb; ++b) {
-            start[b] = run;
-            g.offsets[b] = run;
-            g.counts[b] = total[b];
-            run += total[b];
+    // Order of the variant runs: for a batch the folded decode kernel takes,
+    // the best of blockDim.x * kOrderTries candidate orders (ties go to the
+    // lowest candidate, so the result does not depend on timing); otherwise
+    // the id order.
+    __shared__ unsigned long long red[32];
+    __shared__ int best_cand;
+    int present[kFoldMaxSlots];
+    int D = 0;
+    for (int v = 0; v < V && D <= kFoldMaxSlots; ++v)
+        if (total[v + 1] > 0) {
+            if (D < kFoldMaxSlots) present[D] = v;
+            ++D;
         }
-        g.offsets[nb] = run;
-        // segment plan: present variants, padded segments, passes
+    const int C = pad16(M) / 16;
+    const bool search = D >= 2 && D <= kFoldMaxSlots && C <= kFoldChunks;
+    unsigned long long key = ~0ull;
+    if (search)
+        for (int k = 0; k < kOrderTries; ++k) {
+            const int cand = threadIdx.x * kOrderTries + k;
+            int ord[kFoldMaxSlots];
+            run_order(cand, present, D, ord);
+            const unsigned long long kk = (static_cast<unsigned long long>(order_score(ord, D, total, total[0], C)) << 32) |
+                                          static_cast<unsigned>(cand);
+            key = kk < key ? kk : key;
+        }
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
+        key = other < key ? other : key;
+    }
+    if (lane == 0) red[warp] = key;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned long long b = ~0ull;
+        for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) b = red[w] < b ? red[w] : b;
+        best_cand = search ? static_cast<int>(b & 0xffffffffu) : 0;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // bucket order: base tokens, the variant runs, invalid ids
+        int ord[BITDELTA_MAX_VARIANTS];
+        int n = 0;
+        if (search) {
+            run_order(best_cand, present, D, ord);
+            n = D;
+        } else {
+            for (int v = 0; v < V; ++v)
+                if (total[v + 1] > 0) ord[n++] = v;
+        }
+        int run = total[0];
+        start[0] = 0;
+        for (int k = 0; k < n; ++k) {
+            start[ord[k] + 1] = run;
+            run += total[ord[k] + 1];
+        }
+        for (int v = 0; v < V; ++v)
+            if (total[v + 1] == 0) start[v + 1] = run;
+        start[V + 1] = run;
+        for (int b = 0; b < nb; ++b) {
+            g.offsets[b] = start[b];
+            g.counts[b] = total[b];
+        }
+        g.offsets[nb] = run + total[V + 1];
+        // segment plan: present variants in layout order, padded segments, passes
         SegPlan* pl = g.plan;
         pl->M = M;
         pl->n_base = total[0];
         pl->n_invalid = total[V + 1];
         int d = 0, rows = 0, groups = 0, group_rows = 0, group_vars = 0;
         pl->group_first[0] = 0;
-        for (int v = 0; v < V; ++v) {
+        for (int k = 0; k < n; ++k) {
+            const int v = ord[k];
             const int c = total[v + 1];
-            if (c == 0) continue;
             const int pr = pad16(c);
             if (group_rows > 0 && (group_rows + pr > group_budget || group_vars == kMaxPassVariants)) {
                 pl->group_first[++groups] = d;
@@ -401,7 +518,7 @@ bd_status launch_group(const int32_t* ids, int64_t M, int32_t V, const LinearWor
                        cudaStream_t s) {
     int threads = static_cast<int>(round_up(static_cast<size_t>(M), 32));
     if (threads > 1024) threads = 1024;
-    if (threads < 32) threads = 32;
+    if (threads < 256) threads = 256;            // at least 256 candidate orders
     const size_t smem = sizeof(int) * (32 * (V + 2) + 3 * (V + 2));
     group_kernel<<<1, threads, smem, s>>>(ids, static_cast<int>(M), V, decode_group_budget(M), w.g,
                                           w.status);

@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             prefetch_tensormap(&p.tm_x);
             for (int kb = 0; kb < nkb; ++kb) {
                 const int s = kb % kStages;
-                if (!mbar_wait(&bar_empty[s], ((kb / kStages) & 1) ^ 1, kWaitLimit, p.status, 11, p.diag)) break;
+                if (!mbar_wait_sleep(&bar_empty[s], ((kb / kStages) & 1) ^ 1, kWaitLimit, p.status, 11, p.diag)) break;
                 mbar_expect_tx(&bar_full[s], kStageBytes);
                 uint8_t* st = base + s * kStageBytes;
                 tma_load_2d(st, &p.tm_w, &bar_full[s], kb * kBK, n0);
@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             bool ok = true;
             for (int kb = 0; kb < nkb && ok; ++kb) {
                 const int s = kb % kStages;
-                if (!(ok = mbar_wait(&bar_built[s], (kb / kStages) & 1, kWaitLimit, p.status, 12, p.diag))) break;
+                if (!(ok = mbar_wait_sleep(&bar_built[s], (kb / kStages) & 1, kWaitLimit, p.status, 12, p.diag))) break;
                 tc_fence_after();
                 const uint32_t sa = smem_u32(base + s * kStageBytes);
                 const uint32_t sb = sa + kBN * 128;
@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             const int s = kb % kStages;
             uint2 wbits = make_uint2(0, 0);
             if (bits && row_ok) wbits = __ldg(reinterpret_cast<const uint2*>(bits + static_cast<int64_t>(n) * words_per_row) + kb);
-            if (!(ok = mbar_wait(&bar_full[s], (kb / kStages) & 1, kWaitLimit, p.status, 13, p.diag))) break;
+            if (!(ok = mbar_wait_sleep(&bar_full[s], (kb / kStages) & 1, kWaitLimit, p.status, 13, p.diag))) break;
             if (bits) {
                 uint8_t* row = base + s * kStageBytes + r * 128;
 #pragma unroll
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_built[s]);
         }
-        if (ok && mbar_wait(&acc_full, 0, kWaitLimit, p.status, 14, p.diag)) {
+        if (ok && mbar_wait_sleep(&acc_full, 0, kWaitLimit, p.status, 14, p.diag)) {
             tc_fence_after();
             const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
             for (int c0 = 0; c0 < kBT && pos0 + c0 < pos_end; c0 += 16) {

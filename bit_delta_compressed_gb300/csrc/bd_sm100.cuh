@@ -76,6 +76,18 @@ __device__ __forceinline__ bool mbar_try_wait_ns(uint64_t* bar, uint32_t parity,
     return ok != 0;
 }
 
+// Single-thread bounded wait that suspends up to 1 us per try: a producer
+// lane polling without the hint would keep issuing instructions and take
+// issue slots from the warps sharing its scheduler.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t limit,
+                                                unsigned* status, unsigned where, unsigned* diag) {
+    for (uint32_t i = 0; i < limit; ++i)
+        if (mbar_try_wait_ns(bar, parity, 1000)) return true;
+    if (status) report(status, BD_ERR_TIMEOUT);
+    if (diag) atomicCAS(diag, 0u, where);
+    return false;
+}
+
 // Warp-wide bounded wait: lane 0 alone polls (suspending up to 1 us per try,
 // so waiting warps take no issue slots), the result is broadcast to the warp.
 // Gives up after `limit` tries like mbar_wait.
