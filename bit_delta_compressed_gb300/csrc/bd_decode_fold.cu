@@ -69,6 +69,7 @@ constexpr int kBaseWarp = 3;                    // the base-product issuer
 constexpr int kFirstGroup = 4;                  // warps 0, 1, 2: W, activation and bits producers
 constexpr int kThreads = 32 * (kFirstGroup + kIss * kGroupWarps);
 constexpr int kABufs = 2;                       // +-1 tile buffers per group
+constexpr int kRegEntries = 6;                  // entries whose MMA operands an issuer keeps in registers
 constexpr int kSCol0 = kFoldMaxCols;            // sign accumulator after the base accumulator
 constexpr int kACol0 = 2 * kFoldMaxCols;        // +-1 tiles after both accumulators
 constexpr int kAEntries = (512 - kACol0) / (8 * kABufs);   // entries whose tiles fit
@@ -190,6 +191,21 @@ __device__ void group_issue(const FoldParams& p, const FoldPlan& fp, uint32_t tm
     const int lane = threadIdx.x & 31;
     const bool work = ne > 0;
     const int Mb = p.Mb;
+    // Operands of up to kRegEntries entries live in registers: the D column,
+    // the low word of the B descriptor at stage 0 and step 0 (the stage and
+    // step add 16-byte units to the start-address field; every address stays
+    // below 256 KB, so the field never carries), and the instruction descriptor.
+    const bool in_regs = ne <= kRegEntries;
+    uint32_t r_d[kRegEntries], r_b[kRegEntries], r_id[kRegEntries];
+    const uint64_t xdesc = desc_sw128(smem_u32(xring));
+    const uint32_t xdesc_lo = static_cast<uint32_t>(xdesc), xdesc_hi = static_cast<uint32_t>(xdesc >> 32);
+#pragma unroll
+    for (int k = 0; k < kRegEntries; ++k) {
+        const int e = e0 + (k < ne ? k : 0);
+        r_d[k] = tmem + kSCol0 + fp.e_col[e];
+        r_b[k] = xdesc_lo + static_cast<uint32_t>(Mb + fp.e_row[e]) * 8u;
+        r_id[k] = idesc_e4m3(128, fp.e_n[e]);
+    }
     bool ok = true;
     for (int i = 0; i < nkb; ++i) {
         const int xs = i % p.xstages;
@@ -199,7 +215,20 @@ __device__ void group_issue(const FoldParams& p, const FoldPlan& fp, uint32_t tm
             // releases: an early arrival would count towards a later phase
             if (ok && j == 0) ok = warp_wait(&x_full[xs], (i / p.xstages) & 1, kWaitLimit, p.status, 26, p.diag);
             if (!ok) continue;
-            if (work) {
+            if (work && in_regs) {
+                tc_fence_after();
+                const uint32_t abuf = abase + j * 8 * ne;
+                const uint32_t soff = (static_cast<uint32_t>(xs) * xs_bytes >> 4) + 2u * j;
+#pragma unroll
+                for (int k = 0; k < kRegEntries; ++k)
+                    if (k < ne) {
+                        const uint32_t blo = r_b[k] + soff;
+                        mma_e4m3_ts(r_d[k], abuf + 8 * k, (static_cast<uint64_t>(xdesc_hi) << 32) | blo, r_id[k]);
+                        mma_e4m3_ts(r_d[k], abuf + 8 * k, (static_cast<uint64_t>(xdesc_hi) << 32) | (blo + 4u), r_id[k]);
+                    }
+                commit_elect(&ge[j]);
+                if (j == 1) commit_elect(&x_empty[xs]);
+            } else if (work) {
                 tc_fence_after();
                 const uint32_t sxp = smem_u32(xring + xs * xs_bytes) + Mb * 128;
                 const uint32_t abuf = abase + j * 8 * ne;
