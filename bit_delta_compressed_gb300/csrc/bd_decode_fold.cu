@@ -146,7 +146,6 @@ __device__ __forceinline__ void named_sync(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 constexpr int kGroupThreads = 32 * kGroupWarps;
-constexpr unsigned kFull = 0xffffffffu;
 // Named barrier of group g's +-1 tile buffer b (barrier 0 is __syncthreads).
 __device__ __forceinline__ int group_bar(int g, int b) { return 1 + kABufs * g + b; }
 
