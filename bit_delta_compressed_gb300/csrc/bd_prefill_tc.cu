@@ -265,9 +265,14 @@ size_t tc_scratch_bytes(int64_t M, int64_t N, int64_t K, int32_t V) {
 
 bd_path choose_path(const LinearArgs& a) {
     if (a.M <= 4) return BD_PATH_SIMT;            // GEMV: streams W_base at HBM speed
-    // one variant: the per-variant sign kernel's lighter set-up wins; two or
-    // more: the folded kernel (one accumulator, issuer groups)
-    if (a.V >= 2 && decode_fold_supported(a)) return BD_PATH_DECODE_FOLD;
+    // Measured on GB300 (q, k/v, gate and 4096 x 4096 shapes, 2 to 14 Zipf
+    // variants, 16 to 128 tokens): the per-variant sign kernel wins for few
+    // variants or few tokens; the folded kernel, whose cost hardly grows with
+    // the number of variants, wins from 32 tokens on once there are 8 or more
+    // variants, and from 32 tokens on for narrow outputs (N <= 2048) whatever
+    // the variant count.
+    if (a.V >= 2 && a.M >= 32 && (a.V >= 8 || a.N <= 2048) && decode_fold_supported(a))
+        return BD_PATH_DECODE_FOLD;
     if (decode_tc_supported(a)) return BD_PATH_DECODE_TC;
     if (prefill_tc_supported(a)) return BD_PATH_PREFILL_TC;
     return BD_PATH_SIMT;
