@@ -589,14 +589,6 @@ __global__ void __launch_bounds__(kThreads, 1) fold_decode_kernel(const __grid_c
 //       tokens, zero rows and zero alpha), clamped to [-64, 64];
 //   the split-K tickets zeroed.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t to_e4m3(float v) {
-    return static_cast<uint32_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
-}
-__device__ __forceinline__ float from_e4m3(uint32_t b) {
-    __half_raw hr = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(b), __NV_E4M3);
-    return __half2float(__half(hr));
-}
-
 // Largest |x| of a bf16 row (bf16 bit patterns without the sign order like
 // magnitudes), reduced over the block.
 __device__ float row_absmax(const uint4* __restrict__ src, int64_t vec_per_row) {
@@ -691,33 +683,45 @@ __global__ void __launch_bounds__(256) fold_prep_kernel(const uint4* __restrict_
     const float alpha = alphas[var];
     const int s = scale_exponent(alpha, row_absmax(src, vec_per_row));
     const float sc = pow2i(s);
-    for (int blk = threadIdx.x; blk < K / 64; blk += blockDim.x) {
-        uint32_t w[32];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint4 v = __ldg(src + 8 * blk + i);
-            w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
-        }
-        uint32_t hi[16], lo[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) { hi[i] = 0; lo[i] = 0; }
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {                    // source column c of the block
-            const float xv = (c & 1) ? bf16_hi(w[c >> 1]) : bf16_lo(w[c >> 1]);
-            const float v = (alpha * xv) * sc;
-            const uint32_t h8 = to_e4m3(v);
-            const uint32_t l8 = to_e4m3(v - from_e4m3(h8));
-            const int wd = c >> 5, cc = c & 31;            // word, column within it
-            const int byte = 32 * wd + 4 * (cc & 7) + (cc >> 3);
-            hi[byte >> 2] |= h8 << (8 * (byte & 3));
-            lo[byte >> 2] |= l8 << (8 * (byte & 3));
-        }
-        uint4* o = dst + 8 * blk;
+    // one thread per 32-column group: 64 source bytes in, 32 bytes of hi and
+    // 32 of lo out; output word jj holds columns jj, jj + 8, jj + 16, jj + 24
+    // (converted two at a time)
+    uint8_t* dstb = reinterpret_cast<uint8_t*>(dst);
+    for (int grp = threadIdx.x; grp < K / 32; grp += blockDim.x) {
+        float v[32];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            o[i] = make_uint4(hi[4 * i], hi[4 * i + 1], hi[4 * i + 2], hi[4 * i + 3]);
-            o[4 + i] = make_uint4(lo[4 * i], lo[4 * i + 1], lo[4 * i + 2], lo[4 * i + 3]);
+            const uint4 q = __ldg(src + 4 * grp + i);
+            const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                v[8 * i + 2 * k] = (alpha * bf16_lo(w4[k])) * sc;
+                v[8 * i + 2 * k + 1] = (alpha * bf16_hi(w4[k])) * sc;
+            }
         }
+        uint32_t hi[8], lo[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+            uint32_t hw = 0, lw = 0;
+#pragma unroll
+            for (int pr = 0; pr < 2; ++pr) {               // columns jj + 16 pr and jj + 16 pr + 8
+                const float a0 = v[jj + 16 * pr], a1 = v[jj + 16 * pr + 8];
+                const __nv_fp8x2_storage_t h2 = __nv_cvt_float2_to_fp8x2(make_float2(a0, a1), __NV_SATFINITE, __NV_E4M3);
+                const float2 hb = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(h2, __NV_E4M3)));
+                const __nv_fp8x2_storage_t l2 =
+                    __nv_cvt_float2_to_fp8x2(make_float2(a0 - hb.x, a1 - hb.y), __NV_SATFINITE, __NV_E4M3);
+                hw |= static_cast<uint32_t>(h2) << (16 * pr);
+                lw |= static_cast<uint32_t>(l2) << (16 * pr);
+            }
+            hi[jj] = hw;
+            lo[jj] = lw;
+        }
+        uint4* oh = reinterpret_cast<uint4*>(dstb + 128 * (grp >> 1) + 32 * (grp & 1));
+        uint4* ol = reinterpret_cast<uint4*>(dstb + 128 * (grp >> 1) + 64 + 32 * (grp & 1));
+        oh[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        oh[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+        ol[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        ol[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
     }
 }
 
