@@ -54,7 +54,7 @@ def parse_args():
     p.add_argument("--variants", type=int, default=14)
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-rows", action="store_true", help="skip the compress/prefill/single rows")
-    p.add_argument("--only", choices=["compress", "prefill", "single"], default=None,
+    p.add_argument("--only", choices=["compress", "prefill", "single", "alpha_rows"], default=None,
                    help="run just one row (for profiling); prints only that row")
     p.add_argument("--compress-variants", type=int, default=14)
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -429,8 +429,9 @@ def time_events(torch, fn, iters, stream):
     return a.elapsed_time(b) / iters
 
 
-def run_rows(args, torch, bd, wl, dev, pk, which=("compress", "prefill", "single")):
-    """Compress, prefill and the single-linear decode on their own workloads."""
+def run_rows(args, torch, bd, wl, dev, pk, which=("compress", "prefill", "single", "alpha_rows")):
+    """Compress, prefill, the single-linear decode and the per-row-scale
+    linear on their own workloads."""
     rows = {}
     g = wl.generator(args.seed + 50, dev)
     if "compress" in which:
@@ -441,6 +442,9 @@ def run_rows(args, torch, bd, wl, dev, pk, which=("compress", "prefill", "single
         torch.cuda.empty_cache()
     if "single" in which:
         rows["single4096"] = row_single(args, torch, bd, wl, dev, pk, g)
+        torch.cuda.empty_cache()
+    if "alpha_rows" in which:
+        rows["alpha_rows"] = row_alpha_rows(args, torch, bd, wl, dev, pk, g)
     return rows
 
 
@@ -533,6 +537,50 @@ def row_single(args, torch, bd, wl, dev, pk, g):
         ach = byt / (ms / 1e3) / 1e9
         single["M=%d" % M] = {"us": ms * 1e3, "achieved_gbs": ach, "frac": ach / pk["hbm_gbs"]}
     return single
+
+
+def row_alpha_rows(args, torch, bd, wl, dev, pk, g):
+    """One scale per (variant, output row): the gate shape (28672 x 8192), 14
+    variants, 128 tokens with Zipf(1.1) ids, through ``bitdelta_linear_rows``
+    (grouping included in every call, as for a single linear), beside the
+    per-matrix call with the same ids and path.  4 weight sets rotate (> 2x L2)."""
+    stream = torch.cuda.current_stream()
+    N, K, V, M = 28672, 8192, 14, 128
+    sets = 4
+    ids = wl.variant_ids_zipf(M, V, 1.1, wl.generator(args.seed + 7)).to(dev)
+    D = int(torch.unique(ids[ids >= 0]).numel())
+    mats = []
+    for _ in range(sets):
+        w = wl.base_weights(N, K, g, dev)
+        b = [torch.randint(-2 ** 31, 2 ** 31, (N, K // 32), generator=g, device=dev,
+                           dtype=torch.int64).to(torch.int32) for _ in range(V)]
+        ar = (5e-4 + 1.5e-3 * torch.rand((V, N), generator=g, device=dev)).contiguous()
+        mats.append((w, b, bd.bits_pointer_array(b), ar, ar[:, 0].contiguous()))
+    x = wl.activations(M, K, g, dev)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    ws = bd.linear_workspace(M, N, K, V, dev)
+    path = "auto" if args.path == "auto" else args.path
+
+    def run_rows_all():
+        for w, b, p, ar, _ in mats:
+            bd.linear_rows(x, ids, w, ar, b, out=y, out_dtype=torch.bfloat16, workspace=ws, path=path,
+                           bits_ptrs=p)
+
+    def run_matrix_all():
+        for w, b, p, _, a1 in mats:
+            bd.linear(x, ids, w, a1, b, out=y, out_dtype=torch.bfloat16, workspace=ws, path=path,
+                      bits_ptrs=p)
+    run_rows_all()
+    run_matrix_all()
+    torch.cuda.synchronize()
+    ms_r = time_events(torch, run_rows_all, 5, stream) / sets
+    ms_m = time_events(torch, run_matrix_all, 5, stream) / sets
+    byt = linear_bytes(M, N, K, D) + D * N * 4
+    ach = byt / (ms_r / 1e3) / 1e9
+    return {"workload": "gate 28672x8192, 14 variants (Zipf 1.1), 128 tokens, per-row scales",
+            "us": ms_r * 1e3, "per_matrix_us": ms_m * 1e3, "path": path, "distinct_variants": D,
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": ach / pk["hbm_gbs"], "alg_bytes_per_launch": byt, "traffic": None}}
 
 
 def pick_path(bd, preferred, call):

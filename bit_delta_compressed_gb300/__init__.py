@@ -51,6 +51,8 @@ SIGNATURES = {
     "bitdelta_group": (_ST, [_P, _I64, _I32, _P, _SZ, _P]),
     "bitdelta_linear_grouped": (_ST, [_P, _I64, _I64, _I64, _P, _P, _P, _I32, _P, _ST, _P, _SZ,
                                       _P, _ST]),
+    "bitdelta_linear_rows": (_ST, [_P, _P, _I64, _I64, _I64, _P, _P, _P, _I32, _P, _ST, _P, _SZ,
+                                   _P, _ST]),
     "bitdelta_device_status": (_ST, [_P, _P]),
     "bitdelta_check_bounded_wait": (_ST, [_P, ctypes.c_uint32, ctypes.c_int, _P]),
     "bitdelta_status_string": (ctypes.c_char_p, [_ST]),
@@ -201,6 +203,32 @@ def linear(x, variant_ids, w_base, alphas, bits_list, out_dtype=None, workspace=
                                  al, ctypes.cast(ptrs, ctypes.c_void_p), V, y.data_ptr(),
                                  _dtype_code(out_dtype), ws.data_ptr(), ws.numel(),
                                  _stream(stream), PATHS[path]), "bitdelta_linear")
+    return y
+
+
+def linear_rows(x, variant_ids, w_base, alpha_rows, bits_list, out_dtype=None, workspace=None,
+                out=None, path: str = "auto", stream=None, bits_ptrs=None):
+    """y [M, N] with one scale per (variant, output row): ``alpha_rows`` is a
+    float32 [V, N] device tensor (see ``bitdelta_linear_rows``)."""
+    torch = _torch()
+    _need_cuda(x, variant_ids, w_base)
+    M, K = x.shape
+    N = w_base.shape[0]
+    V = len(bits_list)
+    if V > MAX_VARIANTS:
+        raise ValueError("at most %d variants" % MAX_VARIANTS)
+    if V > 0 and (alpha_rows.dtype != torch.float32 or alpha_rows.numel() != V * N
+                  or not alpha_rows.is_contiguous()):
+        raise ValueError("alpha_rows must be a contiguous float32 [V, N] tensor")
+    out_dtype = out_dtype or torch.float32
+    y = torch.empty((M, N), dtype=out_dtype, device=x.device) if out is None else out
+    ws = linear_workspace(M, N, K, V, x.device) if workspace is None else workspace
+    ptrs = bits_pointer_array(bits_list) if bits_ptrs is None else bits_ptrs
+    al = alpha_rows.data_ptr() if V > 0 else None
+    check(get_lib().bitdelta_linear_rows(x.data_ptr(), variant_ids.data_ptr(), M, N, K, w_base.data_ptr(),
+                                         al, ctypes.cast(ptrs, ctypes.c_void_p), V, y.data_ptr(),
+                                         _dtype_code(out_dtype), ws.data_ptr(), ws.numel(),
+                                         _stream(stream), PATHS[path]), "bitdelta_linear_rows")
     return y
 
 

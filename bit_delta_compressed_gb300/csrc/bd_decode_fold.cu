@@ -8,18 +8,19 @@
 //
 // Per output row n and token t (grouped order) the kernel accumulates, in
 // tensor memory,
-//   B[n, t] = sum_k W[n,k] (x[t,k] 2^s_t)             (base accumulator)
-//   S[n, t] = sum_k s_v[n,k] (alpha_v x[t,k] 2^s_t)    (sign accumulator)
-//   y[t, n] = 2^-s_t (B[n, t] + S[n, t])
-// where 2^s_t is a per-token power of two (exact) that puts the largest
-// |alpha_v x[t,k]| 2^s_t in [128, 256).  The base operand is the bf16
-// activation row scaled by 2^s_t (exact); the sign operand is alpha_v x 2^s_t
-// written as the sum of two e4m3 terms hi = rn(v), lo = rn(v - hi), which
-// keeps about 8 significant bits of every element (the same order as the
-// bf16 activations themselves).  Folding alpha into the sign operand lets
-// every variant share ONE sign accumulator of pad16(M) columns, so tensor
+//   B[n, t] = sum_k W[n,k] (x[t,k] 2^s_t)          (base accumulator)
+//   S[n, t] = sum_k s_v[n,k] (x[t,k] 2^s_t)        (sign accumulator, v = v(t))
+//   y[t, n] = 2^-s_t (B[n, t] + alpha_v S[n, t])
+// where 2^s_t is a per-token power of two (exact) that puts the token's
+// largest |x[t,k]| 2^s_t in [128, 256), and alpha_v is the variant's scale
+// (one per matrix, or one per output row n).  The base operand is the bf16
+// activation row scaled by 2^s_t (exact); the sign operand is x 2^s_t written
+// as the sum of two e4m3 terms hi = rn(v), lo = rn(v - hi), which keeps about
+// 8 significant bits of every element (the same order as the bf16
+// activations themselves).  Each accumulator column belongs to one token and
+// so to one variant: the sign accumulator is shared by all variants, tensor
 // memory holds 2 x 128 accumulator columns and the rest is free for +-1
-// tiles.
+// tiles, and the scale is applied per column (and row) in the epilogue.
 //
 // One CTA owns 128 output rows (the 128 lanes of tensor memory) and a slice
 // of K (split-K at even 64-column blocks, summed in a fixed order by the CTA
@@ -87,6 +88,9 @@ struct FoldParams {
     const SegPlan* plan;
     const FoldPlan* fold;
     const int32_t* pos2tok;
+    const int32_t* pos_var;                     // grouped position -> variant (-1 base, -2 invalid)
+    const float* alphas;                        // [V], or [V, N] when alpha_rows
+    int alpha_rows;
     const int32_t* sexp;                        // [Mb] scale exponent s per grouped position
     void* y;
     float* part;                                // [splits][M][N] by grouped position
@@ -278,8 +282,8 @@ __device__ __forceinline__ void store_signs(uint32_t taddr, uint32_t w) {
 __device__ void group_expand(const FoldParams& p, const SegPlan& pl, const FoldPlan& fp, uint32_t tmem,
                              uint32_t abase, int e0, int ne, int g, int q4, int n0, int nkb, uint64_t* ge,
                              const uint8_t* bring, uint32_t bstage_bytes, uint64_t* b_full, uint64_t* b_empty,
-                             uint64_t* acc_full, const int32_t* tok_s, const float* scale_s, int split, int bcol,
-                             int bn) {
+                             uint64_t* acc_full, const int32_t* tok_s, const float* scale_s, const int32_t* var_s,
+                             const float* alpha_s, int split, int bcol, int bn) {
     using namespace sm100;
     const int lane = threadIdx.x & 31;
     const int r = 32 * q4 + lane;
@@ -326,7 +330,8 @@ __device__ void group_expand(const FoldParams& p, const SegPlan& pl, const FoldP
             if (lane == 0) mbar_arrive(&b_empty[bs]);
         }
     }
-    // ---- epilogue: y = 2^-s_t (D_base + D_sign) over the group's columns ----
+    // ---- epilogue: y = 2^-s_t (B + alpha_v S) over the group's columns, alpha
+    // the variant's scale (per matrix, or of this output row) ----
     if (ok) ok = warp_wait(acc_full, 0, kWaitLimit, p.status, 29, p.diag);
     if (!ok) return;
     tc_fence_after();
@@ -341,7 +346,12 @@ __device__ void group_expand(const FoldParams& p, const SegPlan& pl, const FoldP
             for (int t = 0; t < 16; ++t) {
                 const int pos = c0 + t;
                 if (pos >= p.M) break;
-                const float d = __uint_as_float(v[t]) + __uint_as_float(u[t]);
+                const int vv = var_s[pos];
+                float d = __uint_as_float(v[t]);
+                if (vv >= 0) {
+                    const float a = p.alpha_rows ? __ldg(p.alphas + static_cast<int64_t>(vv) * p.N + n) : alpha_s[pos];
+                    d = fmaf(a, __uint_as_float(u[t]), d);
+                }
                 const float val = pos < n_valid ? d * scale_s[pos] : 0.f;
                 store_out(p, split, pos, tok_s[pos], n, val);
             }
@@ -362,6 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1) fold_decode_kernel(const __grid_c
     __shared__ int last_cta;
     __shared__ int32_t tok_s[kFoldMaxCols];
     __shared__ float scale_s[kFoldMaxCols];
+    __shared__ int32_t var_s[kFoldMaxCols];
+    __shared__ float alpha_s[kFoldMaxCols];      // per-matrix scale of the position's variant
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Mb = p.Mb;
@@ -404,6 +416,8 @@ __global__ void __launch_bounds__(kThreads, 1) fold_decode_kernel(const __grid_c
     for (int q = threadIdx.x; q < Mb; q += blockDim.x) {
         tok_s[q] = q < p.M ? p.pos2tok[q] : -1;
         scale_s[q] = pow2i(-p.sexp[q]);
+        var_s[q] = q < p.M ? p.pos_var[q] : -2;
+        alpha_s[q] = (!p.alpha_rows && var_s[q] >= 0) ? p.alphas[var_s[q]] : 0.f;
     }
     tc_fence_before();
     __syncthreads();
@@ -507,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1) fold_decode_kernel(const __grid_c
                         &drain);
         else
             group_expand(p, pl, fp, tmem, abase, e0, ne, g, warp % 4, n0, nkb, g_empty[g], bring, bstage_bytes,
-                         b_full, b_empty, &acc_full, tok_s, scale_s, split, bcol, bn);
+                         b_full, b_empty, &acc_full, tok_s, scale_s, var_s, alpha_s, split, bcol, bn);
     }
 
     __syncthreads();
@@ -582,11 +596,11 @@ __global__ void __launch_bounds__(kThreads, 1) fold_decode_kernel(const __grid_c
 //       valid tokens);
 //   X_p [R, 2K] bytes: entry rows of the plan; row j of entry e holds, if
 //       grouped position e_col + j is a token of the entry's variant v,
-//       alpha_v x[t] 2^s_t as e4m3 hi and lo, per 64-column block 64 bytes
-//       of hi then 64 of lo, byte 32w + 4j + b of a half holding column
-//       32w + j + 8b; otherwise zeros;
-//   s_t = 7 - floor(log2(|alpha_v| max_k |x[t,k]|)) (0 for base-model
-//       tokens, zero rows and zero alpha), clamped to [-64, 64];
+//       x[t] 2^s_t as e4m3 hi and lo, per 64-column block 64 bytes of hi then
+//       64 of lo, byte 32w + 4j + b of a half holding column 32w + j + 8b;
+//       otherwise zeros;
+//   s_t = 7 - floor(log2(max_k |x[t,k]|)) (0 for zero rows), clamped to
+//       [-64, 64];
 //   the split-K tickets zeroed.
 // ---------------------------------------------------------------------------
 // Largest |x| of a bf16 row (bf16 bit patterns without the sign order like
@@ -609,16 +623,16 @@ __device__ float row_absmax(const uint4* __restrict__ src, int64_t vec_per_row) 
     return __uint_as_float(all << 16);
 }
 
-__device__ __forceinline__ int scale_exponent(float alpha, float xmax) {
-    const float prod = fabsf(alpha) * xmax;
-    if (!(prod > 0.f) || !(prod < 3.0e38f)) return 0;
-    const int biased = static_cast<int>((__float_as_uint(prod) >> 23) & 0xFF);
+// s with 2^s xmax in [128, 256) (0 for a zero or non-finite maximum),
+// clamped to [-64, 64].
+__device__ __forceinline__ int scale_exponent(float xmax) {
+    if (!(xmax > 0.f) || !(xmax < 3.0e38f)) return 0;
+    const int biased = static_cast<int>((__float_as_uint(xmax) >> 23) & 0xFF);
     const int e = biased > 0 ? biased - 127 : -127;
     return max(-64, min(64, 7 - e));
 }
 
 __global__ void __launch_bounds__(256) fold_prep_kernel(const uint4* __restrict__ x, int K, int M, int Mb,
-                                                        const float* __restrict__ alphas,
                                                         const SegPlan* __restrict__ plan,
                                                         const FoldPlan* __restrict__ fold,
                                                         const int32_t* __restrict__ pos2tok,
@@ -634,7 +648,6 @@ __global__ void __launch_bounds__(256) fold_prep_kernel(const uint4* __restrict_
     if (rr < Mb) {
         const int pos = rr;
         const int tok = pos < n_valid ? pos2tok[pos] : -1;
-        const int var = pos < n_valid ? pos_var[pos] : -2;
         uint4* dst = xc + static_cast<int64_t>(pos) * vec_per_row;
         if (tok < 0) {
             for (int64_t i = threadIdx.x; i < vec_per_row; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
@@ -642,7 +655,7 @@ __global__ void __launch_bounds__(256) fold_prep_kernel(const uint4* __restrict_
             return;
         }
         const uint4* src = x + static_cast<int64_t>(tok) * vec_per_row;
-        const int s = var >= 0 ? scale_exponent(alphas[var], row_absmax(src, vec_per_row)) : 0;
+        const int s = scale_exponent(row_absmax(src, vec_per_row));
         if (threadIdx.x == 0) sexp[pos] = s;
         const float sc = pow2i(s);
         for (int64_t i = threadIdx.x; i < vec_per_row; i += blockDim.x) {
@@ -661,16 +674,13 @@ __global__ void __launch_bounds__(256) fold_prep_kernel(const uint4* __restrict_
     }
     const int r = rr - Mb;
     if (r >= fold->R) return;
-    int tok = -1, var = -1;
+    int tok = -1;
     for (int e = 0; e < fold->n_entries; ++e) {
         const int row0 = fold->e_row[e];
         if (r >= row0 && r < row0 + fold->e_n[e]) {
             const int pos = fold->e_col[e] + (r - row0);
             const int d = fold->e_slot[e];
-            if (pos >= plan->off[d] && pos < plan->off[d] + plan->cnt[d]) {
-                tok = pos2tok[pos];
-                var = plan->var[d];
-            }
+            if (pos >= plan->off[d] && pos < plan->off[d] + plan->cnt[d]) tok = pos2tok[pos];
             break;
         }
     }
@@ -680,8 +690,7 @@ __global__ void __launch_bounds__(256) fold_prep_kernel(const uint4* __restrict_
         return;
     }
     const uint4* src = x + static_cast<int64_t>(tok) * vec_per_row;
-    const float alpha = alphas[var];
-    const int s = scale_exponent(alpha, row_absmax(src, vec_per_row));
+    const int s = scale_exponent(row_absmax(src, vec_per_row));
     const float sc = pow2i(s);
     // one thread per 32-column group: 64 source bytes in, 32 bytes of hi and
     // 32 of lo out; output word jj holds columns jj, jj + 8, jj + 16, jj + 24
@@ -695,8 +704,8 @@ __global__ void __launch_bounds__(256) fold_prep_kernel(const uint4* __restrict_
             const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                v[8 * i + 2 * k] = (alpha * bf16_lo(w4[k])) * sc;
-                v[8 * i + 2 * k + 1] = (alpha * bf16_hi(w4[k])) * sc;
+                v[8 * i + 2 * k] = bf16_lo(w4[k]) * sc;
+                v[8 * i + 2 * k + 1] = bf16_hi(w4[k]) * sc;
             }
         }
         uint32_t hi[8], lo[8];
@@ -838,7 +847,7 @@ bd_status launch_decode_fold(const LinearArgs& a, const LinearWorkspace& w, cuda
     if (sc.bytes > w.tc_bytes) return BD_ERR_WORKSPACE;
     const int rmax = fold_rmax(a.M, a.V);
 
-    fold_prep_kernel<<<Mb + rmax, 256, 0, s>>>(static_cast<const uint4*>(a.x), K, M, Mb, a.alphas, w.g.plan,
+    fold_prep_kernel<<<Mb + rmax, 256, 0, s>>>(static_cast<const uint4*>(a.x), K, M, Mb, w.g.plan,
                                               w.g.fold, w.g.pos2tok, w.g.pos_var, sc.sexp,
                                               reinterpret_cast<uint4*>(sc.xc), reinterpret_cast<uint4*>(sc.xp),
                                               sc.tickets, splits > 1 ? static_cast<int>(n_tiles) : 0);
@@ -856,6 +865,9 @@ bd_status launch_decode_fold(const LinearArgs& a, const LinearWorkspace& w, cuda
     p.plan = w.g.plan;
     p.fold = w.g.fold;
     p.pos2tok = w.g.pos2tok;
+    p.pos_var = w.g.pos_var;
+    p.alphas = a.alphas;
+    p.alpha_rows = a.alpha_rows;
     p.sexp = sc.sexp;
     p.y = a.y;
     p.part = sc.part;

@@ -63,7 +63,8 @@ struct DecodeParams {
     CUtensorMap tm_xp;                    // X_p [P_bound, 2K] bytes (e4m3 hi|lo per 64-col block), box 16 rows
     CUtensorMap tm_xp128;                 // the same, box 128 rows
     CUtensorMap tm_bits[BITDELTA_MAX_VARIANTS];   // packed bits [N, K/32] u32, box 128 rows x 4 words
-    const float* alphas;
+    const float* alphas;                        // [V], or [V, N] when alpha_rows
+    int alpha_rows;
     const SegPlan* plan;
     const int32_t* pos2tok;
     const int32_t* sigma;                 // per token
@@ -184,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     __syncthreads();
     // per grouped position: token and the epilogue's scale of the sign product
     for (int d = 0; d < pl.D; ++d) {
-        const float alpha = p.alphas[pl.var[d]];
+        const float alpha = p.alpha_rows ? 1.f : p.alphas[pl.var[d]];    // per-row scales: in the epilogue
         for (int j = threadIdx.x; j < pl.cnt[d]; j += blockDim.x) {
             const int pos = pl.off[d] + j;
             const int tok = p.pos2tok[pos];
@@ -373,6 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             }
             for (int d = q.d0; d < q.d1; ++d) {
                 const int cnt = pl.cnt[d], off = pl.off[d];
+                const float ar = (p.alpha_rows && row_ok) ? p.alphas[static_cast<int64_t>(pl.var[d]) * p.N + n] : 1.f;
                 const uint32_t scol = kBaseCol + Mb + (pl.seg[d] - q.row0);
                 for (int ci = h; 8 * ci < cnt; ci += 2) {
                     const int pos0 = off + 8 * ci;
@@ -386,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                         for (int t = 0; t < 8; ++t) {
                             if (8 * ci + t >= cnt) break;
                             store_y(p, split, tok_s[pos0 + t], n,
-                                    fmaf(scale_s[pos0 + t], __uint_as_float(sg[t]), __uint_as_float(bs[t])));
+                                    fmaf(ar * scale_s[pos0 + t], __uint_as_float(sg[t]), __uint_as_float(bs[t])));
                         }
                     }
                 }
@@ -630,6 +632,7 @@ bd_status launch_decode_tc(const LinearArgs& a, const LinearWorkspace& w, cudaSt
     for (int v = 0; v < a.V; ++v)
         if (!make_tmap_bits(&p.tm_bits[v], a.bits.p[v], a.N, a.K / 32, kBN)) return BD_ERR_CUDA;
     p.alphas = a.alphas;
+    p.alpha_rows = a.alpha_rows;
     p.plan = w.g.plan;
     p.pos2tok = w.g.pos2tok;
     p.sigma = sc.sigma;

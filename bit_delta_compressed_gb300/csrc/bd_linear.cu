@@ -196,7 +196,7 @@ __device__ int order_score(const int* ord, int D, const int* total, int n_base, 
 }
 
 __global__ void __launch_bounds__(1024) group_kernel(const int32_t* __restrict__ ids, int M, int V,
-                                                     int group_budget, GroupView g,
+                                                     int group_budget, int order_search, GroupView g,
                                                      unsigned* status) {
     extern __shared__ int sm[];
     const int nb = V + 2;
@@ -214,8 +214,8 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t* __restrict__
         atomicAdd(&total[b], 1);
     }
     if (__syncthreads_or(bad) && threadIdx.x == 0) report(status, BD_ERR_VARIANT);
-    // Order of the variant runs: for a batch the folded decode kernel takes,
-    // the best of blockDim.x * kOrderTries candidate orders (ties go to the
+    // Order of the variant runs: for a batch the folded decode kernel may
+    // take (the caller says whether it can), the best of blockDim.x * kOrderTries candidate orders (ties go to the
     // lowest candidate, so the result does not depend on timing); otherwise
     // the id order.
     __shared__ unsigned long long red[32];
@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t* __restrict__
             ++D;
         }
     const int C = pad16(M) / 16;
-    const bool search = D >= 2 && D <= kFoldMaxSlots && C <= kFoldChunks;
+    const bool search = order_search && D >= 2 && D <= kFoldMaxSlots && C <= kFoldChunks;
     unsigned long long key = ~0ull;
     if (search)
         for (int k = 0; k < kOrderTries; ++k) {
@@ -345,7 +345,7 @@ constexpr int kSimtTok = 8;
 
 __global__ void __launch_bounds__(kSimtWarps * 32)
 simt_linear_kernel(const uint4* __restrict__ x, const uint4* __restrict__ w_base,
-                   const float* __restrict__ alphas, BitsTable bt, int64_t M, int64_t N,
+                   const float* __restrict__ alphas, int alpha_rows, BitsTable bt, int64_t M, int64_t N,
                    int64_t K, GroupView g, void* y, int y_bf16) {
     const int lane = threadIdx.x & 31;
     const int64_t n = static_cast<int64_t>(blockIdx.x) * kSimtWarps + (threadIdx.x >> 5);
@@ -403,7 +403,7 @@ simt_linear_kernel(const uint4* __restrict__ x, const uint4* __restrict__ w_base
             for (int j = 0; j < kSimtTok; ++j) {
                 if (tok[j] < 0) continue;
                 float out = 0.f;
-                if (var[j] >= 0) out = fmaf(alphas[var[j]], accs[j], accb[j]);
+                if (var[j] >= 0) out = fmaf(alpha_rows ? alphas[var[j] * N + n] : alphas[var[j]], accs[j], accb[j]);
                 else if (var[j] == -1) out = accb[j];
                 const int64_t o = static_cast<int64_t>(tok[j]) * N + n;
                 if (y_bf16) static_cast<__nv_bfloat16*>(y)[o] = __float2bfloat16_rn(out);
@@ -422,7 +422,7 @@ simt_linear_kernel(const uint4* __restrict__ x, const uint4* __restrict__ w_base
 template <int MT, int U>
 __global__ void __launch_bounds__(kSimtWarps * 32)
 gemv_kernel(const uint4* __restrict__ x, const uint4* __restrict__ w_base,
-            const float* __restrict__ alphas, BitsTable bt, int M, int64_t N, int64_t K,
+            const float* __restrict__ alphas, int alpha_rows, BitsTable bt, int M, int64_t N, int64_t K,
             GroupView g, void* y, int y_bf16) {
     const int lane = threadIdx.x & 31;
     const int64_t n = static_cast<int64_t>(blockIdx.x) * kSimtWarps + (threadIdx.x >> 5);
@@ -505,7 +505,7 @@ gemv_kernel(const uint4* __restrict__ x, const uint4* __restrict__ w_base,
             if (j >= M) continue;
             const int t = g.pos2tok[j];
             float out = 0.f;
-            if (var[j] >= 0) out = fmaf(alphas[var[j]], accs[j], accb[j]);
+            if (var[j] >= 0) out = fmaf(alpha_rows ? alphas[var[j] * N + n] : alphas[var[j]], accs[j], accb[j]);
             else if (var[j] == -1) out = accb[j];
             const int64_t o = static_cast<int64_t>(t) * N + n;
             if (y_bf16) static_cast<__nv_bfloat16*>(y)[o] = __float2bfloat16_rn(out);
@@ -515,13 +515,13 @@ gemv_kernel(const uint4* __restrict__ x, const uint4* __restrict__ w_base,
 }
 
 bd_status launch_group(const int32_t* ids, int64_t M, int32_t V, const LinearWorkspace& w,
-                       cudaStream_t s) {
+                       cudaStream_t s, bool order_search) {
     int threads = static_cast<int>(round_up(static_cast<size_t>(M), 32));
     if (threads > 1024) threads = 1024;
-    if (threads < 256) threads = 256;            // at least 256 candidate orders
+    if (order_search && threads < 256) threads = 256;        // at least 256 candidate orders
     const size_t smem = sizeof(int) * (32 * (V + 2) + 3 * (V + 2));
-    group_kernel<<<1, threads, smem, s>>>(ids, static_cast<int>(M), V, decode_group_budget(M), w.g,
-                                          w.status);
+    group_kernel<<<1, threads, smem, s>>>(ids, static_cast<int>(M), V, decode_group_budget(M),
+                                          order_search ? 1 : 0, w.g, w.status);
     return launch_status();
 }
 
@@ -533,13 +533,13 @@ bd_status launch_simt(const LinearArgs& a, const LinearWorkspace& w, cudaStream_
         const int M = static_cast<int>(a.M);
         const int yb = a.y_dtype == BD_BF16;
         const unsigned grid = static_cast<unsigned>(blocks);
-        if (a.M == 1) gemv_kernel<1, 4><<<grid, kSimtWarps * 32, 0, s>>>(xx, wb, a.alphas, a.bits, M, a.N, a.K, w.g, a.y, yb);
-        else if (a.M == 2) gemv_kernel<2, 4><<<grid, kSimtWarps * 32, 0, s>>>(xx, wb, a.alphas, a.bits, M, a.N, a.K, w.g, a.y, yb);
-        else gemv_kernel<4, 2><<<grid, kSimtWarps * 32, 0, s>>>(xx, wb, a.alphas, a.bits, M, a.N, a.K, w.g, a.y, yb);
+        if (a.M == 1) gemv_kernel<1, 4><<<grid, kSimtWarps * 32, 0, s>>>(xx, wb, a.alphas, a.alpha_rows, a.bits, M, a.N, a.K, w.g, a.y, yb);
+        else if (a.M == 2) gemv_kernel<2, 4><<<grid, kSimtWarps * 32, 0, s>>>(xx, wb, a.alphas, a.alpha_rows, a.bits, M, a.N, a.K, w.g, a.y, yb);
+        else gemv_kernel<4, 2><<<grid, kSimtWarps * 32, 0, s>>>(xx, wb, a.alphas, a.alpha_rows, a.bits, M, a.N, a.K, w.g, a.y, yb);
         return launch_status();
     }
     simt_linear_kernel<<<static_cast<unsigned>(blocks), kSimtWarps * 32, 0, s>>>(
-        static_cast<const uint4*>(a.x), static_cast<const uint4*>(a.w_base), a.alphas, a.bits,
+        static_cast<const uint4*>(a.x), static_cast<const uint4*>(a.w_base), a.alphas, a.alpha_rows, a.bits,
         a.M, a.N, a.K, w.g, a.y, a.y_dtype == BD_BF16);
     return launch_status();
 }
@@ -579,7 +579,7 @@ extern "C" size_t bitdelta_linear_workspace(int64_t M, int64_t N, int64_t K, int
 namespace {
 
 bd_status prepare(const void* x, int64_t M, int64_t N, int64_t K, const void* w_base,
-                  const float* alphas, const uint32_t* const* bits, int32_t V, void* y,
+                  const float* alphas, int alpha_rows, const uint32_t* const* bits, int32_t V, void* y,
                   bd_dtype y_dtype, void* workspace, size_t ws_bytes, bd_path& path,
                   LinearArgs& a, LinearWorkspace& w) {
     if (!workspace) return BD_ERR_WORKSPACE;
@@ -592,6 +592,7 @@ bd_status prepare(const void* x, int64_t M, int64_t N, int64_t K, const void* w_
     a.K = K;
     a.w_base = w_base;
     a.alphas = alphas;
+    a.alpha_rows = alpha_rows;
     a.V = V;
     for (int v = 0; v < BITDELTA_MAX_VARIANTS; ++v)
         a.bits.p[v] = (v < V) ? reinterpret_cast<const uint8_t*>(bits[v]) : nullptr;
@@ -630,7 +631,7 @@ extern "C" bd_status bitdelta_group(const int32_t* variant_ids, int64_t M, int32
     if (!aligned(workspace, 16)) return BD_ERR_ALIGN;
     LinearWorkspace w = linear_workspace_layout(workspace, M, 1, 32, V);
     if (ws_bytes < w.group_end) return BD_ERR_WORKSPACE;
-    return launch_group(variant_ids, M, V, w, static_cast<cudaStream_t>(stream));
+    return launch_group(variant_ids, M, V, w, static_cast<cudaStream_t>(stream), true);
 }
 
 extern "C" bd_status bitdelta_linear_grouped(const void* x, int64_t M, int64_t N, int64_t K,
@@ -645,7 +646,7 @@ extern "C" bd_status bitdelta_linear_grouped(const void* x, int64_t M, int64_t N
     LinearArgs a;
     LinearWorkspace w;
     a.ids = nullptr;
-    st = prepare(x, M, N, K, w_base, alphas, bits, V, y, y_dtype, workspace, ws_bytes, path, a, w);
+    st = prepare(x, M, N, K, w_base, alphas, 0, bits, V, y, y_dtype, workspace, ws_bytes, path, a, w);
     if (st != BD_OK) return st;
     return launch_path(path, a, w, static_cast<cudaStream_t>(stream));
 }
@@ -661,10 +662,29 @@ extern "C" bd_status bitdelta_linear_ex(const void* x, const int32_t* variant_id
     LinearArgs a;
     LinearWorkspace w;
     a.ids = variant_ids;
-    st = prepare(x, M, N, K, w_base, alphas, bits, V, y, y_dtype, workspace, ws_bytes, path, a, w);
+    st = prepare(x, M, N, K, w_base, alphas, 0, bits, V, y, y_dtype, workspace, ws_bytes, path, a, w);
     if (st != BD_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    st = launch_group(variant_ids, M, V, w, s);
+    st = launch_group(variant_ids, M, V, w, s, path == BD_PATH_DECODE_FOLD);
+    if (st != BD_OK) return st;
+    return launch_path(path, a, w, s);
+}
+
+extern "C" bd_status bitdelta_linear_rows(const void* x, const int32_t* variant_ids, int64_t M,
+                                          int64_t N, int64_t K, const void* w_base,
+                                          const float* alpha_rows, const uint32_t* const* bits,
+                                          int32_t V, void* y, bd_dtype y_dtype, void* workspace,
+                                          size_t ws_bytes, void* stream, bd_path path) {
+    bd_status st = check_linear_args(x, variant_ids, M, N, K, w_base, alpha_rows, bits, V, y, y_dtype);
+    if (st != BD_OK) return st;
+    if (M == 0) return BD_OK;
+    LinearArgs a;
+    LinearWorkspace w;
+    a.ids = variant_ids;
+    st = prepare(x, M, N, K, w_base, alpha_rows, 1, bits, V, y, y_dtype, workspace, ws_bytes, path, a, w);
+    if (st != BD_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    st = launch_group(variant_ids, M, V, w, s, path == BD_PATH_DECODE_FOLD);
     if (st != BD_OK) return st;
     return launch_path(path, a, w, s);
 }

@@ -16,7 +16,8 @@ struct LinearArgs {
     const int32_t* ids;              // [M]
     int64_t M, N, K;
     const void* w_base;              // bf16 [N, K]
-    const float* alphas;             // [V]
+    const float* alphas;             // [V], or [V, N] when alpha_rows
+    int32_t alpha_rows;              // 1: one scale per (variant, output row)
     int32_t V;
     BitsTable bits;
     const uint32_t* const* bits_host;

@@ -43,7 +43,8 @@ struct PrefillParams {
     CUtensorMap tm_w;                       // W_base [N, K]
     CUtensorMap tm_x;                       // grouped activations [Mpad, K]
     const uint32_t* bits[BITDELTA_MAX_VARIANTS];
-    const float* alphas;
+    const float* alphas;                        // [V], or [V, N] when alpha_rows
+    int alpha_rows;
     const SegPlan* plan;
     const int32_t* pos2tok;
     void* y;
@@ -158,7 +159,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const int n = n0 + r;
         const bool row_ok = n < p.N;
         const uint32_t* bits = var >= 0 ? p.bits[var] : nullptr;
-        const float alpha = var >= 0 ? p.alphas[var] : 0.f;
+        const float alpha = var < 0 ? 0.f
+                            : p.alpha_rows ? (row_ok ? p.alphas[static_cast<int64_t>(var) * p.N + n] : 0.f)
+                                           : p.alphas[var];
         const uint32_t abits = __float_as_uint(alpha);
         const int words_per_row = p.K / 32;
         bool ok = true;
@@ -295,6 +298,7 @@ bd_status launch_prefill_tc(const LinearArgs& a, const LinearWorkspace& w, cudaS
         return BD_ERR_CUDA;
     for (int v = 0; v < a.V; ++v) p.bits[v] = reinterpret_cast<const uint32_t*>(a.bits.p[v]);
     p.alphas = a.alphas;
+    p.alpha_rows = a.alpha_rows;
     p.plan = w.g.plan;
     p.pos2tok = w.g.pos2tok;
     p.y = a.y;

@@ -72,9 +72,9 @@ typedef enum {
     BD_PATH_SIMT = 1,       /* CUDA-core kernel, any M */
     BD_PATH_DECODE_TC = 2,  /* tcgen05 decode kernel: base and sign products on tensor cores */
     BD_PATH_PREFILL_TC = 3, /* tcgen05 prefill kernel: W_eff tiles built in shared memory */
-    BD_PATH_DECODE_FOLD = 4 /* tcgen05 decode kernel, alpha folded into the sign operand so the
-                               base and sign products share one accumulator (M <= 128 and at
-                               most 16 distinct variants per batch) */
+    BD_PATH_DECODE_FOLD = 4 /* tcgen05 decode kernel with one sign accumulator shared by all
+                               variants (a column per token), the scales applied in the epilogue:
+                               M <= 128 tokens and at most 16 distinct variants */
 } bd_path;
 
 /* ------------------------------------------------------------------ */
@@ -198,6 +198,22 @@ bd_status bitdelta_linear_ex(const void *x, const int32_t *variant_ids,
                              void *y, bd_dtype y_dtype,
                              void *workspace, size_t ws_bytes, void *stream,
                              bd_path path);
+
+/* The fused linear with one scale per (variant, output row) ("Infrastructure
+ * details": the scales are stored as f32, one per output dimension), the
+ * form bitdelta_compress_rows produces:
+ *   y[t, n] = sum_k x[t,k] * (W_base[n,k] + alpha_rows[v(t) * N + n] * s_{v(t)}[n,k]).
+ *   alpha_rows : device, float [V, N] row-major (variant v's scales start at
+ *                alpha_rows + v * N), 4-byte aligned.
+ * Other arguments, layouts, ownership, errors and kernel paths as
+ * bitdelta_linear_ex (every path takes per-row scales). */
+bd_status bitdelta_linear_rows(const void *x, const int32_t *variant_ids,
+                               int64_t M, int64_t N, int64_t K,
+                               const void *w_base, const float *alpha_rows,
+                               const uint32_t *const *bits, int32_t V,
+                               void *y, bd_dtype y_dtype,
+                               void *workspace, size_t ws_bytes, void *stream,
+                               bd_path path);
 
 /* ------------------------------------------------------------------ */
 /* Status                                                               */

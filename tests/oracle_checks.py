@@ -222,6 +222,38 @@ def check_closed_form_linear(o):
         assert np.array_equal(y[t], exact), (t, v)
 
 
+def check_closed_form_linear_rows(o):
+    # per-row scales ("Infrastructure details": one f32 per output dimension):
+    # delta_v[n, :] = +-c_{v,n} with c on a dyadic grid, different for every
+    # (variant, row); bitdelta's row compression recovers c exactly, the
+    # reconstruction with per-row scales is exact (W_eff == W_ft) and y is an
+    # exact integer sum.  Catches a wrong (variant, row) index of the scales.
+    rng = np.random.default_rng(18)
+    M, N, K, V = 6, 20, 64, 3
+    wb_i = rng.integers(-64, 65, size=(N, K))                 # W_base = wb_i * 2^-10
+    wb32 = (wb_i * 2.0 ** -10).astype(np.float32)
+    arows, bits, wft_i = [], [], []
+    for v in range(V):
+        c = rng.integers(1, 16, size=N) * 2.0 ** -14          # c_{v,n}
+        s = rng.choice([-1, 1], size=(N, K))
+        wf32 = (wb32.astype(np.float64) + c[:, None] * s).astype(np.float32)
+        a64, a32, b = o.compress_rows(wf32, wb32)
+        assert np.array_equal(a64, c)
+        arows.append(a32)
+        bits.append(b)
+        wft_i.append(np.round(wf32.astype(np.float64) * 2 ** 14).astype(np.int64))
+    x_i = rng.integers(-8, 9, size=(M, K))                   # x = x_i * 2^-3
+    x = to_bf16_bits(x_i * 0.125)
+    vid = np.array([2, 0, -1, 1, 2, 0], dtype=np.int32)
+    y = o.linear(x, vid, to_bf16_bits(wb32), np.stack(arows).astype(np.float32), bits,
+                 per_row_alpha=True)
+    for t in range(M):
+        v = vid[t]
+        w = (wb_i * 16) if v < 0 else wft_i[v]               # units of 2^-14
+        exact = (x_i[t][None, :] * w).sum(axis=1) * 2.0 ** -17
+        assert np.array_equal(y[t], exact), (t, v)
+
+
 def check_zero_delta_linear(o):
     rng = np.random.default_rng(9)
     M, N, K = 5, 40, 128

@@ -34,6 +34,9 @@ MUTANTS = [
     ("base_variant_gets_scale", "w_eff[k] = wb;\n", "w_eff[k] = wb + (double)j->alphas[0];\n"),
     ("first_variant_scale_for_all", ": (double)j->alphas[v];", ": (double)j->alphas[0];"),
     ("first_variant_bits_for_all", "sign_bit(j->bits[v], K, n, k)", "sign_bit(j->bits[0], K, n, k)"),
+    ("row_scale_index_swapped", "(double)j->alphas[(int64_t)v * j->N + n]",
+     "(double)j->alphas[(n * j->V + v) % (j->V * j->N)]"),
+    ("row_scale_first_row", "(double)j->alphas[(int64_t)v * j->N + n]", "(double)j->alphas[(int64_t)v * j->N]"),
     ("output_transposed_store", "j->y[t * j->nrows + ri] = acc;",
      "j->y[(ri * j->M + t) % (j->M * j->nrows)] = acc;"),
 ]
