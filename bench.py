@@ -54,7 +54,7 @@ def parse_args():
     p.add_argument("--variants", type=int, default=14)
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-rows", action="store_true", help="skip the compress/prefill/single rows")
-    p.add_argument("--only", choices=["compress", "prefill", "single", "alpha_rows"], default=None,
+    p.add_argument("--only", choices=["compress", "prefill", "single", "alpha_rows", "reconstruct"], default=None,
                    help="run just one row (for profiling); prints only that row")
     p.add_argument("--compress-variants", type=int, default=14)
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -429,9 +429,10 @@ def time_events(torch, fn, iters, stream):
     return a.elapsed_time(b) / iters
 
 
-def run_rows(args, torch, bd, wl, dev, pk, which=("compress", "prefill", "single", "alpha_rows")):
-    """Compress, prefill, the single-linear decode and the per-row-scale
-    linear on their own workloads."""
+def run_rows(args, torch, bd, wl, dev, pk,
+             which=("compress", "prefill", "single", "alpha_rows", "reconstruct")):
+    """Compress, prefill, the single-linear decode, the per-row-scale linear
+    and the materialised reconstruction on their own workloads."""
     rows = {}
     g = wl.generator(args.seed + 50, dev)
     if "compress" in which:
@@ -445,6 +446,9 @@ def run_rows(args, torch, bd, wl, dev, pk, which=("compress", "prefill", "single
         torch.cuda.empty_cache()
     if "alpha_rows" in which:
         rows["alpha_rows"] = row_alpha_rows(args, torch, bd, wl, dev, pk, g)
+        torch.cuda.empty_cache()
+    if "reconstruct" in which:
+        rows["reconstruct"] = row_reconstruct(args, torch, bd, wl, dev, pk, g)
     return rows
 
 
@@ -581,6 +585,59 @@ def row_alpha_rows(args, torch, bd, wl, dev, pk, g):
             "us": ms_r * 1e3, "per_matrix_us": ms_m * 1e3, "path": path, "distinct_variants": D,
             "roofline": {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": ach / pk["hbm_gbs"], "alg_bytes_per_launch": byt, "traffic": None}}
+
+
+def row_reconstruct(args, torch, bd, wl, dev, pk, g):
+    """Materialised W_eff: 14 variants of one 28672 x 8192 matrix rebuilt in
+    bf16 (HBM roofline, 4.125 bytes per weight); then the gate decode workload
+    (14 Zipf variants, 128 tokens) as "reconstruct, then a library GEMM"
+    (torch.matmul per present variant and one for base-model tokens) beside
+    the fused linear on the same inputs."""
+    stream = torch.cuda.current_stream()
+    N, K, V, M = 28672, 8192, 14, 128
+    wb = wl.base_weights(N, K, g, dev)
+    bits = [torch.randint(-2 ** 31, 2 ** 31, (N, K // 32), generator=g, device=dev,
+                          dtype=torch.int64).to(torch.int32) for _ in range(V)]
+    alphas = 1e-3 * (1 + torch.rand(V, generator=g, device=dev))
+    w_eff = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+
+    def rec_all():
+        for v in range(V):
+            bd.reconstruct(wb, alphas[v:v + 1], bits[v], out=w_eff)
+    rec_all()
+    ms_rec = time_events(torch, rec_all, 5, stream)
+    per = 2 * N * K + N * K // 8 + 2 * N * K
+    ach = V * per / (ms_rec / 1e3) / 1e9
+    ids = wl.variant_ids_zipf(M, V, 1.1, wl.generator(args.seed + 7)).to(dev)
+    x = wl.activations(M, K, g, dev)
+    groups = [(v, torch.nonzero(ids == v).flatten()) for v in range(V)]
+    groups = [(v, idx) for v, idx in groups if idx.numel() > 0]
+    base_idx = torch.nonzero(ids < 0).flatten()
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+
+    def materialise_then_gemm():
+        for v, idx in groups:
+            bd.reconstruct(wb, alphas[v:v + 1], bits[v], out=w_eff)
+            y[idx] = torch.matmul(x[idx], w_eff.t())
+        if base_idx.numel():
+            y[base_idx] = torch.matmul(x[base_idx], wb.t())
+    ws = bd.linear_workspace(M, N, K, V, dev)
+    ptrs = bd.bits_pointer_array(bits)
+    y2 = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+
+    def fused():
+        bd.linear(x, ids, wb, alphas, bits, out=y2, out_dtype=torch.bfloat16, workspace=ws, bits_ptrs=ptrs)
+    materialise_then_gemm()
+    fused()
+    torch.cuda.synchronize()
+    ms_mat = time_events(torch, materialise_then_gemm, 3, stream)
+    ms_fused = time_events(torch, fused, 5, stream)
+    return {"workload": "14 variants of 28672x8192; gate decode 128 tokens, 14 Zipf variants",
+            "ms": ms_rec, "launches": V,
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": ach / pk["hbm_gbs"], "alg_bytes_per_launch": per, "traffic": None},
+            "decode_gate_materialise_then_gemm_ms": ms_mat, "decode_gate_fused_ms": ms_fused,
+            "fused_speedup": ms_mat / ms_fused, "distinct_variants": len(groups)}
 
 
 def pick_path(bd, preferred, call):

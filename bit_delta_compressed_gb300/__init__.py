@@ -44,6 +44,7 @@ SIGNATURES = {
     "bitdelta_compress": (_ST, [_P, _P, _ST, _I64, _I64, _P, _P, _P, _SZ, _P]),
     "bitdelta_compress_rows": (_ST, [_P, _P, _ST, _I64, _I64, _P, _P, _P]),
     "bitdelta_compress_noalloc": (_ST, [_P, _P, _ST, _I64, _I64, _P, _P, _P]),
+    "bitdelta_reconstruct": (_ST, [_P, _P, _I32, _P, _I64, _I64, _P, _P]),
     "bitdelta_linear_workspace": (_SZ, [_I64, _I64, _I64, _I32]),
     "bitdelta_linear": (_ST, [_P, _P, _I64, _I64, _I64, _P, _P, _P, _I32, _P, _ST, _P, _SZ, _P]),
     "bitdelta_linear_ex": (_ST, [_P, _P, _I64, _I64, _I64, _P, _P, _P, _I32, _P, _ST, _P, _SZ,
@@ -168,6 +169,21 @@ def compress_rows(w_ft, w_base, stream=None):
                                      N, K, alpha.data_ptr(), bits.data_ptr(), _stream(stream)),
           "bitdelta_compress_rows")
     return alpha, bits
+
+
+def reconstruct(w_base, alpha, bits, out=None, stream=None):
+    """bf16 W_eff [N, K] = nearest bf16 of W_base + alpha * s (``alpha``: a
+    float32 tensor of 1 or N values; see ``bitdelta_reconstruct``)."""
+    torch = _torch()
+    _need_cuda(w_base, alpha, bits)
+    N, K = w_base.shape
+    if alpha.dtype != torch.float32 or alpha.numel() not in (1, N) or not alpha.is_contiguous():
+        raise ValueError("alpha must be a contiguous float32 tensor of 1 or N values")
+    per_row = 1 if (alpha.numel() == N and N != 1) else 0
+    out = torch.empty((N, K), dtype=torch.bfloat16, device=w_base.device) if out is None else out
+    check(get_lib().bitdelta_reconstruct(w_base.data_ptr(), alpha.data_ptr(), per_row, bits.data_ptr(), N, K,
+                                         out.data_ptr(), _stream(stream)), "bitdelta_reconstruct")
+    return out
 
 
 def linear_workspace(M: int, N: int, K: int, V: int, device=None):

@@ -132,6 +132,25 @@ bd_status bitdelta_compress_noalloc(const void *w_ft, const void *w_base, bd_dty
                                     int64_t N, int64_t K, float *alpha_out,
                                     uint32_t *bits_out, void *stream);
 
+/* Materialised effective weights of one variant ("Serving architecture":
+ * the conceptual listing rebuilds W_eff in the base dtype and hands it to a
+ * standard linear; "Latency profile": reconstruction in prefill, then the
+ * standard matmul).  The fused linear below never needs this; it exists so
+ * that "reconstruct, then a library GEMM" can run beside the fused path.
+ *   W_eff[n,k] = bf16(W_base[n,k] + a * s[n,k]), rounded to nearest (ties to
+ *   even) from the exact sum; a = alpha[0] (per_row == 0) or alpha[n]
+ *   (per_row != 0); s = +1 where the stored bit is 1, -1 where it is 0.
+ *   w_base    : device, bf16 [N, K] row-major, 16-byte aligned.
+ *   alpha     : device, float [1] or [N].
+ *   bits      : device, [N, K/32] words as bitdelta_compress writes them.
+ *   w_eff_out : device, bf16 [N, K], 16-byte aligned, not overlapping w_base.
+ *   N >= 1, K >= 32, K % 32 == 0.
+ * Returns BD_OK, or an argument error (overlap: BD_ERR_ALIGN) with nothing
+ * launched. */
+bd_status bitdelta_reconstruct(const void *w_base, const float *alpha, int32_t per_row,
+                               const uint32_t *bits, int64_t N, int64_t K,
+                               void *w_eff_out, void *stream);
+
 /* ------------------------------------------------------------------ */
 /* Multi-variant fused linear ("Serving architecture": W_eff =         */
 /* W_base + alpha_v * sign(delta_v), reconstructed on the fly and fused */

@@ -74,6 +74,8 @@ class Oracle:
             fn.restype = ctypes.c_int
         L.bdo_compress_rows.argtypes = [_p, _p, ctypes.c_int, _i64, _i64, _p, _p, _p]
         L.bdo_compress_rows.restype = ctypes.c_int
+        L.bdo_reconstruct.argtypes = [_p, _p, ctypes.c_int, _p, _i64, _i64, _p]
+        L.bdo_reconstruct.restype = ctypes.c_int
         L.bdo_linear.argtypes = [_p, _p, _i64, _i64, _i64, _p, _p, ctypes.c_int,
                                  _p, ctypes.c_int32, _p, _i64, _p, ctypes.c_int]
         L.bdo_linear.restype = ctypes.c_int
@@ -117,6 +119,22 @@ class Oracle:
         return a64, a32, bits
 
     # -- multi-variant linear --------------------------------------------
+    def reconstruct(self, w_base: np.ndarray, alpha, bits: np.ndarray, per_row: bool = False) -> np.ndarray:
+        """bf16 bits [N, K] of the nearest bf16 (ties to even) of
+        W_base + a * s, a = alpha (scalar) or alpha[n] with ``per_row``."""
+        w_base = np.ascontiguousarray(w_base, dtype=np.uint16)
+        bits = np.ascontiguousarray(bits, dtype=np.uint32)
+        N, K = w_base.shape
+        al = np.ascontiguousarray(np.atleast_1d(alpha), dtype=np.float32)
+        if bits.shape != (N, K // 32) or al.shape[0] != (N if per_row else 1):
+            raise ValueError("shape mismatch")
+        out = np.empty((N, K), dtype=np.uint16)
+        rc = self.lib.bdo_reconstruct(w_base.ctypes.data, al.ctypes.data, int(per_row), bits.ctypes.data, N, K,
+                                      out.ctypes.data)
+        if rc != 0:
+            raise ValueError("oracle reconstruct failed: %d" % rc)
+        return out
+
     def linear(self, x: np.ndarray, variant_ids: np.ndarray, w_base: np.ndarray,
                alphas: np.ndarray, bits: list, rows=None, nthreads: int | None = None,
                per_row_alpha: bool = False) -> np.ndarray:

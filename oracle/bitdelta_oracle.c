@@ -122,6 +122,45 @@ int bdo_compress_rows(const void *w_ft, const void *w_base, int is_bf16,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Materialised reconstruction.                                             */
+/* "Serving architecture": the conceptual listing rebuilds                  */
+/* W_eff = W_base + alpha * sign(delta) in the base dtype (bf16 here).      */
+/* w_eff[n,k] = nearest bf16 (ties to even) of W_base[n,k] + a * s[n,k],    */
+/* a = alpha[0] or alpha[n]; the sum is exact in fp64 whenever the two      */
+/* terms' exponents differ by less than 29 (always for these workloads).    */
+/* Values stay in the normal binary32 range.                                */
+/* Pinned: exact closed form, hand-computed ties, exact rational rounding.  */
+/* ------------------------------------------------------------------------ */
+
+static uint16_t nearest_bf16(double d)
+{
+    if (d == 0.0) return signbit(d) ? (uint16_t)0x8000u : (uint16_t)0u;
+    int e;
+    double m = frexp(fabs(d), &e);              /* |d| = m 2^e, m in [0.5, 1) */
+    double q = nearbyint(m * 256.0);            /* 8 significant bits, ties to even */
+    float f = (float)ldexp(q, e - 8);           /* exact: at most 9 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    uint16_t h = (uint16_t)(u >> 16);
+    return d < 0.0 ? (uint16_t)(h | 0x8000u) : h;
+}
+
+int bdo_reconstruct(const uint16_t *w_base, const float *alpha, int per_row,
+                    const uint32_t *bits, int64_t N, int64_t K, uint16_t *w_eff)
+{
+    if (N <= 0 || K <= 0 || K % 32 != 0) return -1;
+    for (int64_t n = 0; n < N; ++n) {
+        double a = (double)alpha[per_row ? n : 0];
+        for (int64_t k = 0; k < K; ++k) {
+            int bit = (int)((bits[(n * K + k) / 32] >> ((n * K + k) % 32)) & 1u);
+            double s = (double)(2 * bit - 1);
+            w_eff[n * K + k] = nearest_bf16(bf16_to_double(w_base[n * K + k]) + a * s);
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Multi-variant linear.                                                    */
 /* "Serving architecture": reconstruct W_eff = W_base + alpha_v * sign(d_v), */
 /* then y = x * W_eff^T (the conceptual fused_bitdelta_linear listing).     */

@@ -25,6 +25,7 @@ import json
 import os
 
 import numpy as np
+from fractions import Fraction
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 
@@ -180,6 +181,74 @@ def check_rows_alpha(o):
     one64, _, _ = o.compress_rows(wf[:1], wb[:1])
     r64, _, _ = o.compress(wf[:1], wb[:1])
     assert one64[0] == r64
+
+
+# -- reconstruction pins ----------------------------------------------------
+
+def check_reconstruct_closed_form(o):
+    # W_base on a 2^-10 grid with |W| <= 2^-6, delta = +-2^-12: every W_ft is a
+    # bf16 value, so W_eff must equal the bf16 W_ft bit for bit.
+    rng = np.random.default_rng(40)
+    N, K = 12, 96
+    wb = rng.integers(-16, 17, size=(N, K)) * 2.0 ** -10
+    s = rng.choice([-1.0, 1.0], size=(N, K))
+    wf = wb + s * 2.0 ** -12
+    a64, a32, bits = o.compress(wf.astype(np.float32), wb.astype(np.float32))
+    assert a64 == 2.0 ** -12
+    out = o.reconstruct(to_bf16_bits(wb), a32, bits)
+    assert np.array_equal(out, to_bf16_bits(wf))
+
+
+def check_reconstruct_ties(o):
+    # hand-computed roundings around 1.0 (bf16 spacing 2^-7 above, 2^-8 below)
+    cases = [  # (W_base bits, alpha, bit, expected bits)
+        (0x3F80, 2.0 ** -8, 1, 0x3F80),                 # 1 + 2^-8: tie, to even 1.0
+        (0x3F81, 2.0 ** -8, 1, 0x3F82),                 # 1.0078125 + 2^-8: tie, to even
+        (0x3F80, 2.0 ** -8 + 2.0 ** -20, 1, 0x3F81),    # just above the tie
+        (0x3F80, 2.0 ** -8 - 2.0 ** -20, 1, 0x3F80),    # just below the tie
+        (0x3F80, 2.0 ** -8, 0, 0x3F7F),                 # 1 - 2^-8 is a bf16 value
+        (0xBF80, 2.0 ** -8, 0, 0xBF80),                 # -1 - 2^-8: tie, to even -1.0
+        (0xBF80, 2.0 ** -8 + 2.0 ** -20, 0, 0xBF81),    # beyond the tie, away from zero
+    ]
+    for wbits, alpha, bit, want in cases:
+        wb = np.full((1, 32), wbits, dtype=np.uint16)
+        bits = np.full((1, 1), 0xFFFFFFFF if bit else 0, dtype=np.uint32)
+        got = o.reconstruct(wb, np.float32(alpha), bits)
+        assert np.all(got == want), (hex(wbits), alpha, bit, hex(int(got[0, 0])), hex(want))
+
+
+def _bf16_nearest_exact(value: Fraction) -> int:
+    """Nearest bf16 (ties to even) of an exact rational, by exact arithmetic."""
+    if value == 0:
+        return 0
+    sign = 0x8000 if value < 0 else 0
+    mag = -value if value < 0 else value
+    e = mag.numerator.bit_length() - mag.denominator.bit_length()
+    while Fraction(2) ** e > mag:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= mag:
+        e += 1
+    q = round(mag / Fraction(2) ** (e - 7))             # 8 significant bits, half to even
+    v = float(q * Fraction(2) ** (e - 7))
+    return sign | int(np.float32(v).view(np.uint32) >> 16)
+
+
+def check_reconstruct_exact_rational(o):
+    # random Laplace deltas, per-matrix and per-row scales, against exact
+    # rational arithmetic and Python's round-half-even
+    rng = np.random.default_rng(41)
+    N, K = 3, 64
+    wb = to_bf16_bits(rng.normal(0, 0.02, size=(N, K)))
+    bits = rng.integers(0, 2 ** 32, size=(N, K // 32), dtype=np.uint64).astype(np.uint32)
+    for per_row in (False, True):
+        alpha = rng.uniform(1e-4, 3e-3, size=N if per_row else 1).astype(np.float32)
+        out = o.reconstruct(wb, alpha, bits, per_row=per_row)
+        s = unpack_ref(bits, K)                              # +-1
+        for n in range(N):
+            a = Fraction(float(alpha[n if per_row else 0]))
+            for k in range(K):
+                exact = Fraction(float(bf16_bits_to_f64(wb[n, k]))) + a * int(s[n, k])
+                assert out[n, k] == _bf16_nearest_exact(exact), (per_row, n, k)
 
 
 # -- linear pins -------------------------------------------------------------

@@ -36,6 +36,10 @@ MUTANTS = [
     ("first_variant_bits_for_all", "sign_bit(j->bits[v], K, n, k)", "sign_bit(j->bits[0], K, n, k)"),
     ("row_scale_index_swapped", "(double)j->alphas[(int64_t)v * j->N + n]",
      "(double)j->alphas[(n * j->V + v) % (j->V * j->N)]"),
+    ("reconstruct_ties_away", "double q = nearbyint(m * 256.0);", "double q = floor(m * 256.0 + 0.5);"),
+    ("reconstruct_truncates", "double q = nearbyint(m * 256.0);", "double q = floor(m * 256.0);"),
+    ("reconstruct_row_scale_first", "double a = (double)alpha[per_row ? n : 0];", "double a = (double)alpha[0];"),
+    ("reconstruct_sign_flipped", "double s = (double)(2 * bit - 1);", "double s = (double)(1 - 2 * bit);"),
     ("row_scale_first_row", "(double)j->alphas[(int64_t)v * j->N + n]", "(double)j->alphas[(int64_t)v * j->N]"),
     ("output_transposed_store", "j->y[t * j->nrows + ri] = acc;",
      "j->y[(ri * j->M + t) % (j->M * j->nrows)] = acc;"),
