@@ -359,13 +359,14 @@ def run_ours(args, rank, world, local_rank):
                             else "fallback 6.8 TB/s")}
 
     e2e = measure_e2e(args, torch, bd, linears, ids, ws, V, stream)
+    chained = measure_chained(args, torch, bd, linears, ids, ws, V, stream)
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded; random-init 70B-shaped weights, Laplace deltas)",
             "config": stack_config(args, D), "roofline": roof, "e2e": e2e,
-            "gpu_launches": (1 + n_lin) * args.steps, "clocks": clocks}
+            "gpu_launches": (1 + n_lin) * args.steps, "clocks": clocks, "chained": chained}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         dt, w_done, threads = oracle_sample_time(args, wl, args.cpu_sample_rows, args.seed)
@@ -416,6 +417,37 @@ def measure_e2e(args, torch, bd, linears, ids, ws, V, stream):
     ms = a.elapsed_time(b) / n
     return {"value": args.tokens / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+def measure_chained(args, torch, bd, linears, ids, ws, V, stream):
+    """The same stack as real decoder layers: each layer's projections fed by
+    the previous ones (q/k/v from the hidden state, o from q in place of the
+    attention output, gate/up from the residual sum, down from silu(gate) * up,
+    residual adds), the glue in torch; the batch grouped once per step."""
+    from bit_delta_compressed_gb300 import layer
+    per = len(layer.NAMES)
+    layers = []
+    for i in range(0, len(linears), per):
+        chunk = linears[i:i + per]
+        lin = {n: L for n, L in zip(layer.NAMES, chunk)}
+        bufs = {n: L["y"] for n, L in zip(layer.NAMES, chunk)}
+        layers.append((lin, bufs))
+    h0 = linears[0]["x"]
+
+    def chained_step():
+        bd.group(ids, V, ws)
+        h = h0
+        for lin, bufs in layers:
+            h = layer.chained_layer(bd, lin, h, V, ws, bufs, path=args.path)
+        return h
+    for _ in range(2):
+        chained_step()
+    torch.cuda.synchronize()
+    n = max(3, args.steps // 5)
+    ms = time_events(torch, chained_step, n, stream)
+    return {"value": args.tokens / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
+            "dataflow": "q,k,v <- h; o <- q (attention output stand-in); h1 = h + o; "
+                        "gate, up <- h1; down <- silu(gate) * up; h2 = h1 + down (glue in torch)"}
 
 
 def time_events(torch, fn, iters, stream):
