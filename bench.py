@@ -54,7 +54,8 @@ def parse_args():
     p.add_argument("--variants", type=int, default=14)
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-rows", action="store_true", help="skip the compress/prefill/single rows")
-    p.add_argument("--only", choices=["compress", "prefill", "single", "alpha_rows", "reconstruct"], default=None,
+    p.add_argument("--only", choices=["compress", "prefill", "single", "alpha_rows", "reconstruct", "delta_cache"],
+                   default=None,
                    help="run just one row (for profiling); prints only that row")
     p.add_argument("--compress-variants", type=int, default=14)
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -462,7 +463,7 @@ def time_events(torch, fn, iters, stream):
 
 
 def run_rows(args, torch, bd, wl, dev, pk,
-             which=("compress", "prefill", "single", "alpha_rows", "reconstruct")):
+             which=("compress", "prefill", "single", "alpha_rows", "reconstruct", "delta_cache")):
     """Compress, prefill, the single-linear decode, the per-row-scale linear
     and the materialised reconstruction on their own workloads."""
     rows = {}
@@ -481,6 +482,9 @@ def run_rows(args, torch, bd, wl, dev, pk,
         torch.cuda.empty_cache()
     if "reconstruct" in which:
         rows["reconstruct"] = row_reconstruct(args, torch, bd, wl, dev, pk, g)
+        torch.cuda.empty_cache()
+    if "delta_cache" in which:
+        rows["delta_cache"] = row_delta_cache(args, torch, dev)
     return rows
 
 
@@ -670,6 +674,36 @@ def row_reconstruct(args, torch, bd, wl, dev, pk, g):
                          "frac": ach / pk["hbm_gbs"], "alg_bytes_per_launch": per, "traffic": None},
             "decode_gate_materialise_then_gemm_ms": ms_mat, "decode_gate_fused_ms": ms_fused,
             "fused_speedup": ms_mat / ms_fused, "distinct_variants": len(groups)}
+
+
+def row_delta_cache(args, torch, dev):
+    """Delta-cache loads: three variants of 1 GiB of packed bits each (pinned
+    host memory) through a 2 GiB device cache, so every other acquire loads
+    one variant and evicts another; bytes moved host -> device per second on
+    the cache's copy stream."""
+    from bit_delta_compressed_gb300.cache import DeltaCache
+    nbits = 1 << 30
+    cache = DeltaCache(2 * nbits + (1 << 20), dev)
+    for i in range(3):
+        bits = torch.empty(nbits // 4, dtype=torch.int32).pin_memory()
+        bits.fill_(i)
+        cache.register("v%d" % i, [torch.full((1024,), 1e-3).pin_memory()], [bits])
+    order = ["v0", "v1", "v2", "v0", "v1", "v2"]
+    cache.release(cache.acquire("v0"))
+    cache.release(cache.acquire("v1"))
+    torch.cuda.synchronize()
+    before = cache.bytes_loaded
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(cache.copy_stream)
+    for name in order[2:]:
+        cache.release(cache.acquire(name))
+    t1.record(cache.copy_stream)
+    torch.cuda.synchronize()
+    moved = cache.bytes_loaded - before
+    ms = t0.elapsed_time(t1)
+    return {"workload": "3 variants x 1 GiB of bits through a 2 GiB device cache (LRU x rate)",
+            "loads": len(order) - 2, "bytes": moved, "ms": ms, "gbs": moved / (ms / 1e3) / 1e9}
 
 
 def pick_path(bd, preferred, call):
