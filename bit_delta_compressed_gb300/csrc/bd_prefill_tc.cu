@@ -9,14 +9,17 @@
 //
 // With thousands of tokens per variant the work is a dense bf16 contraction
 // per variant, so each W_eff tile is built once in shared memory and reused
-// across a 256-token tile on the tensor cores:
+// across a 512-token tile on the tensor cores (the tile is sized for reuse:
+// per 64-column block a CTA loads 16 KB of W and 64 KB of activations from
+// L2 for 8.4 MFLOP, and the L2-to-SM fill rate, not the tensor pipe, sets
+// the pace):
 //   * a TMA producer loads the W_base tile (128 rows x 64 columns) and the
-//     token tile (256 grouped tokens x 64 columns) of one variant;
+//     token tile (512 grouped tokens x 64 columns, two boxes) of one variant;
 //   * four builder warps (one thread per weight row) rewrite the W tile in
 //     place as bf16(W_base + alpha_v * s_v) from the variant's sign bits,
 //     then hand it to the tensor core (async-proxy fence + mbarrier);
-//   * one thread issues tcgen05.mma (M = 128 weight rows, N = 256 tokens,
-//     fp32 accumulator in tensor memory);
+//   * one thread issues tcgen05.mma (M = 128 weight rows, two MMAs of N = 256
+//     tokens per K step, fp32 accumulators in all 512 tensor-memory columns);
 //   * the builder warps then read the accumulator out and store y rows of
 //     the tokens that belong to the variant.
 // Tokens of the base model (id -1) use W_base unchanged.
@@ -30,12 +33,13 @@ size_t decode_tc_scratch_bytes(int64_t M, int64_t N, int64_t K, int32_t V);
 namespace {
 
 constexpr int kBN = 128;            // weight rows per CTA (MMA M, TMEM lanes)
-constexpr int kBT = 256;            // tokens per CTA (MMA N)
+constexpr int kBT = 512;            // tokens per CTA: two MMAs of N = 256 per K step
+constexpr int kBX = 256;            // tokens per MMA and per activation TMA box
 constexpr int kBK = 64;
-constexpr int kStages = 4;
+constexpr int kStages = 2;
 constexpr int kThreads = 192;       // warp 0 TMA, warp 1 MMA, warps 2..5 build + epilogue
 constexpr int kBuildWarps = 4;
-constexpr int kTmemCols = 256;
+constexpr int kTmemCols = 512;
 constexpr uint32_t kWaitLimit = 1u << 20;
 constexpr uint32_t kStageBytes = kBN * 128 + kBT * 128;
 
@@ -131,12 +135,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                 mbar_expect_tx(&bar_full[s], kStageBytes);
                 uint8_t* st = base + s * kStageBytes;
                 tma_load_2d(st, &p.tm_w, &bar_full[s], kb * kBK, n0);
-                tma_load_2d(st + kBN * 128, &p.tm_x, &bar_full[s], kb * kBK, pos0);
+                for (int h = 0; h < kBT / kBX; ++h)
+                    tma_load_2d(st + kBN * 128 + h * kBX * 128, &p.tm_x, &bar_full[s], kb * kBK, pos0 + h * kBX);
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            const uint32_t idesc = idesc_bf16(kBN, kBT);
+            const uint32_t idesc = idesc_bf16(kBN, kBX);
             bool ok = true;
             for (int kb = 0; kb < nkb && ok; ++kb) {
                 const int s = kb % kStages;
@@ -146,8 +151,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                 const uint32_t sb = sa + kBN * 128;
 #pragma unroll
                 for (int k16 = 0; k16 < 4; ++k16)
-                    mma_ss(tmem, desc_sw128(sa + 32 * k16), desc_sw128(sb + 32 * k16), idesc,
-                           (kb > 0 || k16 > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int h = 0; h < kBT / kBX; ++h)
+                        mma_ss(tmem + h * kBX, desc_sw128(sa + 32 * k16), desc_sw128(sb + h * kBX * 128 + 32 * k16),
+                               idesc, (kb > 0 || k16 > 0) ? 1u : 0u);
                 mma_commit(&bar_empty[s]);
             }
             if (ok) mma_commit(&acc_full);
@@ -294,7 +301,7 @@ bd_status launch_prefill_tc(const LinearArgs& a, const LinearWorkspace& w, cudaS
     PrefillParams p;
     memset(&p, 0, sizeof p);
     if (!make_tmap_bf16_sw128(&p.tm_w, a.w_base, a.N, a.K, kBN) ||
-        !make_tmap_bf16_sw128(&p.tm_x, xg, Mpad, a.K, kBT))
+        !make_tmap_bf16_sw128(&p.tm_x, xg, Mpad, a.K, kBX))
         return BD_ERR_CUDA;
     for (int v = 0; v < a.V; ++v) p.bits[v] = reinterpret_cast<const uint32_t*>(a.bits.p[v]);
     p.alphas = a.alphas;
