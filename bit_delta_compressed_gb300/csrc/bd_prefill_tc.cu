@@ -9,17 +9,19 @@
 //
 // With thousands of tokens per variant the work is a dense bf16 contraction
 // per variant, so each W_eff tile is built once in shared memory and reused
-// across a 512-token tile on the tensor cores (the tile is sized for reuse:
-// per 64-column block a CTA loads 16 KB of W and 64 KB of activations from
-// L2 for 8.4 MFLOP, and the L2-to-SM fill rate, not the tensor pipe, sets
-// the pace):
-//   * a TMA producer loads the W_base tile (128 rows x 64 columns) and the
-//     token tile (512 grouped tokens x 64 columns, two boxes) of one variant;
-//   * four builder warps (one thread per weight row) rewrite the W tile in
+// across the CTA's tokens on the tensor cores.  A CTA covers kRowTiles x 128
+// weight rows and kTokTiles x 256 tokens (all 512 tensor-memory columns); the
+// tile is sized for reuse: per 64-column block it loads 32 KB of W and 32 KB
+// of activations from L2 for 8.4 MFLOP, and the L2-to-SM fill rate, not the
+// tensor pipe, sets the pace:
+//   * a TMA producer loads the W_base tile (256 rows x 64 columns) and the
+//     token tile (256 grouped tokens x 64 columns) of one variant;
+//   * builder warps (one thread per weight row) rewrite the W tile in
 //     place as bf16(W_base + alpha_v * s_v) from the variant's sign bits,
 //     then hand it to the tensor core (async-proxy fence + mbarrier);
-//   * one thread issues tcgen05.mma (M = 128 weight rows, two MMAs of N = 256
-//     tokens per K step, fp32 accumulators in all 512 tensor-memory columns);
+//   * one thread issues tcgen05.mma (M = 128 weight rows per MMA, N = 256
+//     tokens, one MMA per row tile and token tile per K step, fp32
+//     accumulators in tensor memory);
 //   * the builder warps then read the accumulator out and store y rows of
 //     the tokens that belong to the variant.
 // Tokens of the base model (id -1) use W_base unchanged.
@@ -32,16 +34,21 @@ size_t decode_tc_scratch_bytes(int64_t M, int64_t N, int64_t K, int32_t V);
 
 namespace {
 
-constexpr int kBN = 128;            // weight rows per CTA (MMA M, TMEM lanes)
-constexpr int kBT = 512;            // tokens per CTA: two MMAs of N = 256 per K step
-constexpr int kBX = 256;            // tokens per MMA and per activation TMA box
+constexpr int kRowTiles = 2;        // 128-row MMA tiles per CTA (TMEM lanes = rows of one tile)
+constexpr int kTokTiles = 1;        // 256-token MMA tiles per CTA
+constexpr int kBM = 128;            // MMA M
+constexpr int kBX = 256;            // MMA N, and tokens per activation TMA box
+constexpr int kBN = kBM * kRowTiles;    // weight rows per CTA
+constexpr int kBT = kBX * kTokTiles;    // tokens per CTA
 constexpr int kBK = 64;
-constexpr int kStages = 2;
-constexpr int kThreads = 192;       // warp 0 TMA, warp 1 MMA, warps 2..5 build + epilogue
-constexpr int kBuildWarps = 4;
+constexpr int kBuildWarps = 4 * kRowTiles;
+constexpr int kThreads = 64 + 32 * kBuildWarps;   // warp 0 TMA, warp 1 MMA, then build + epilogue
 constexpr int kTmemCols = 512;
 constexpr uint32_t kWaitLimit = 1u << 20;
 constexpr uint32_t kStageBytes = kBN * 128 + kBT * 128;
+constexpr int kStages = (225 * 1024) / kStageBytes < 4 ? (225 * 1024) / kStageBytes : 4;
+static_assert(kRowTiles * kTokTiles * kBX <= kTmemCols, "accumulators must fit tensor memory");
+static_assert(kStages >= 2, "at least two pipeline stages");
 
 struct PrefillParams {
     CUtensorMap tm_w;                       // W_base [N, K]
@@ -141,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            const uint32_t idesc = idesc_bf16(kBN, kBX);
+            const uint32_t idesc = idesc_bf16(kBM, kBX);
             bool ok = true;
             for (int kb = 0; kb < nkb && ok; ++kb) {
                 const int s = kb % kStages;
@@ -152,17 +159,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 #pragma unroll
                 for (int k16 = 0; k16 < 4; ++k16)
 #pragma unroll
-                    for (int h = 0; h < kBT / kBX; ++h)
-                        mma_ss(tmem + h * kBX, desc_sw128(sa + 32 * k16), desc_sw128(sb + h * kBX * 128 + 32 * k16),
-                               idesc, (kb > 0 || k16 > 0) ? 1u : 0u);
+                    for (int rt = 0; rt < kRowTiles; ++rt)
+#pragma unroll
+                        for (int tt = 0; tt < kTokTiles; ++tt)
+                            mma_ss(tmem + kBX * (rt * kTokTiles + tt), desc_sw128(sa + rt * kBM * 128 + 32 * k16),
+                                   desc_sw128(sb + tt * kBX * 128 + 32 * k16), idesc, (kb > 0 || k16 > 0) ? 1u : 0u);
                 mma_commit(&bar_empty[s]);
             }
             if (ok) mma_commit(&acc_full);
         }
     } else {
-        // builder warps: thread r owns weight row r of the tile
+        // builder warps: thread r owns weight row r of the CTA's rows; warp
+        // (q, rt) covers TMEM lane quarter q of row tile rt
         const int q = warp % 4;
-        const int r = 32 * q + lane;
+        const int rt = (warp - 2) / 4;
+        const int r = kBM * rt + 32 * q + lane;
         const int n = n0 + r;
         const bool row_ok = n < p.N;
         const uint32_t* bits = var >= 0 ? p.bits[var] : nullptr;
@@ -206,7 +217,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
             for (int c0 = 0; c0 < kBT && pos0 + c0 < pos_end; c0 += 16) {
                 uint32_t v[16];
-                tmem_ld16(tmem + lane_addr + c0, v);
+                const int col = kBX * (rt * kTokTiles + c0 / kBX) + c0 % kBX;
+                tmem_ld16(tmem + lane_addr + col, v);
                 tmem_ld_wait();
                 if (row_ok) {
 #pragma unroll
@@ -300,6 +312,7 @@ bd_status launch_prefill_tc(const LinearArgs& a, const LinearWorkspace& w, cudaS
     if (launch_status() != BD_OK) return BD_ERR_CUDA;
     PrefillParams p;
     memset(&p, 0, sizeof p);
+    static_assert(kBN <= 256 && kBX <= 256, "TMA boxes are at most 256 rows");
     if (!make_tmap_bf16_sw128(&p.tm_w, a.w_base, a.N, a.K, kBN) ||
         !make_tmap_bf16_sw128(&p.tm_x, xg, Mpad, a.K, kBX))
         return BD_ERR_CUDA;
