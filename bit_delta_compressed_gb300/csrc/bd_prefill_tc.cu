@@ -286,7 +286,10 @@ size_t tc_scratch_bytes(int64_t M, int64_t N, int64_t K, int32_t V) {
 }
 
 bd_path choose_path(const LinearArgs& a) {
-    if (a.M <= 4) return BD_PATH_SIMT;            // GEMV: streams W_base at HBM speed
+    // GEMV (CUDA cores) for 1-2 tokens; from 3 tokens the tensor-core decode
+    // kernel is faster (4096 x 4096: 11.9 / 14.5 / 24.6 / 26.6 us for 1-4
+    // tokens on CUDA cores against 22.5 us on tensor cores)
+    if (a.M <= 2) return BD_PATH_SIMT;
     // Measured on GB300 (q, k/v, gate and 4096 x 4096 shapes, 2 to 14 Zipf
     // variants, 16 to 128 tokens): the per-variant sign kernel wins for few
     // variants or few tokens; the folded kernel, whose cost hardly grows with
