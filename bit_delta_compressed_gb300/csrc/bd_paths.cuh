@@ -36,5 +36,8 @@ size_t decode_fold_scratch_bytes(int64_t M, int64_t N, int64_t K, int32_t V);
 bd_status launch_decode_fold(const LinearArgs& a, const LinearWorkspace& w, cudaStream_t s);
 bd_status launch_decode_tc(const LinearArgs& a, const LinearWorkspace& w, cudaStream_t s);
 bd_status launch_prefill_tc(const LinearArgs& a, const LinearWorkspace& w, cudaStream_t s);
+// W_eff of every variant present in the grouped batch, slot d of the plan at
+// weff + d * N * K (bf16, nearest to the exact sum).
+bd_status launch_reconstruct_plan(const LinearArgs& a, const SegPlan* plan, void* weff, cudaStream_t s);
 
 }  // namespace bd

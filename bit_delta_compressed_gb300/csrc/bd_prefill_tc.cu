@@ -24,7 +24,11 @@
 //     accumulators in tensor memory);
 //   * the builder warps then read the accumulator out and store y rows of
 //     the tokens that belong to the variant.
-// Tokens of the base model (id -1) use W_base unchanged.
+// Tokens of the base model (id -1) use W_base unchanged.  When the average
+// variant of the batch has >= 2048 tokens, every present variant's W_eff is
+// first materialised in the workspace (nearest bf16, one HBM pass per
+// variant) and the kernel loads those tiles ready-made: the in-tile rewrite
+// costs about a quarter of the GEMM time, the pass 4.125 bytes per weight.
 #include "bd_sm100.cuh"
 #include "bd_tc_common.cuh"
 
@@ -53,6 +57,8 @@ static_assert(kStages >= 2, "at least two pipeline stages");
 struct PrefillParams {
     CUtensorMap tm_w;                       // W_base [N, K]
     CUtensorMap tm_x;                       // grouped activations [Mpad, K]
+    CUtensorMap tm_weff[BITDELTA_MAX_VARIANTS];  // materialised W_eff of plan slot d (when prebuilt)
+    int prebuilt;                           // 1: W_eff tiles come ready from HBM, no rewrite
     const uint32_t* bits[BITDELTA_MAX_VARIANTS];
     const float* alphas;                        // [V], or [V, N] when alpha_rows
     int alpha_rows;
@@ -66,12 +72,13 @@ struct PrefillParams {
 
 // Token tile `jt` (in grouped order over base tokens then each variant) ->
 // first grouped position, end position and variant id (-1 = base).
-__device__ bool token_tile(const SegPlan& pl, int jt, int& pos0, int& pos_end, int& var) {
+__device__ bool token_tile(const SegPlan& pl, int jt, int& pos0, int& pos_end, int& var, int& slot) {
     int nt = (pl.n_base + kBT - 1) / kBT;
     if (jt < nt) {
         pos0 = jt * kBT;
         pos_end = pl.n_base;
         var = -1;
+        slot = -1;
         return true;
     }
     jt -= nt;
@@ -81,6 +88,7 @@ __device__ bool token_tile(const SegPlan& pl, int jt, int& pos0, int& pos_end, i
             pos0 = pl.off[d] + jt * kBT;
             pos_end = pl.off[d] + pl.cnt[d];
             var = pl.var[d];
+            slot = d;
             return true;
         }
         jt -= nt;
@@ -112,8 +120,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const int wt_in = min(group_w, p.n_wtiles - grp * group_w);
     const int wt = grp * group_w + rem % wt_in;
     const int jt = rem / wt_in;
-    int pos0 = 0, pos_end = 0, var = -1;
-    if (wt >= p.n_wtiles || jt >= jt_count || !token_tile(pl, jt, pos0, pos_end, var)) return;
+    int pos0 = 0, pos_end = 0, var = -1, slot = -1;
+    if (wt >= p.n_wtiles || jt >= jt_count || !token_tile(pl, jt, pos0, pos_end, var, slot)) return;
+    // W tiles: the variant's materialised W_eff (prebuilt), else W_base
+    // rewritten in shared memory by the builder warps
+    const bool use_weff = p.prebuilt && var >= 0;
+    const CUtensorMap* tmw = use_weff ? &p.tm_weff[slot] : &p.tm_w;
     const int n0 = wt * kBN;
     const int nkb = p.K / kBK;
 
@@ -134,14 +146,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 
     if (warp == 0) {
         if (lane == 0) {
-            prefetch_tensormap(&p.tm_w);
+            prefetch_tensormap(tmw);
             prefetch_tensormap(&p.tm_x);
             for (int kb = 0; kb < nkb; ++kb) {
                 const int s = kb % kStages;
                 if (!mbar_wait_sleep(&bar_empty[s], ((kb / kStages) & 1) ^ 1, kWaitLimit, p.status, 11, p.diag)) break;
                 mbar_expect_tx(&bar_full[s], kStageBytes);
                 uint8_t* st = base + s * kStageBytes;
-                tma_load_2d(st, &p.tm_w, &bar_full[s], kb * kBK, n0);
+                tma_load_2d(st, tmw, &bar_full[s], kb * kBK, n0);
                 for (int h = 0; h < kBT / kBX; ++h)
                     tma_load_2d(st + kBN * 128 + h * kBX * 128, &p.tm_x, &bar_full[s], kb * kBK, pos0 + h * kBX);
             }
@@ -176,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const int r = kBM * rt + 32 * q + lane;
         const int n = n0 + r;
         const bool row_ok = n < p.N;
-        const uint32_t* bits = var >= 0 ? p.bits[var] : nullptr;
+        const uint32_t* bits = (var >= 0 && !use_weff) ? p.bits[var] : nullptr;
         const float alpha = var < 0 ? 0.f
                             : p.alpha_rows ? (row_ok ? p.alphas[static_cast<int64_t>(var) * p.N + n] : 0.f)
                                            : p.alphas[var];
@@ -266,8 +278,24 @@ __global__ void __launch_bounds__(256) gather_x_kernel(const uint4* __restrict__
         xg[row * vec + i] = tok >= 0 ? __ldg(x + tok * vec + i) : make_uint4(0, 0, 0, 0);
 }
 
-size_t prefill_scratch_bytes(int64_t M, int64_t K) {
-    return round_up(static_cast<size_t>(pad16(static_cast<int>(M))) * K * 2, kAlign);
+// Materialise each present variant's W_eff before the GEMM when the average
+// variant has at least this many tokens: rebuilding a W tile in shared memory
+// costs about a quarter of the GEMM time, a reconstruction pass over HBM
+// 4.125 bytes per weight, which is less from ~2000 tokens per variant on.
+constexpr int64_t kMatTokensPerVariant = 2048;
+constexpr int64_t kMatMaxBytes = int64_t(32) << 30;
+
+int64_t mat_slots(int64_t M, int32_t V) { return V < M ? V : M; }
+
+bool materialise(int64_t M, int64_t N, int64_t K, int32_t V) {
+    const int64_t d = mat_slots(M, V);
+    return d >= 1 && M / d >= kMatTokensPerVariant && d * N * K * 2 <= kMatMaxBytes;
+}
+
+size_t prefill_scratch_bytes(int64_t M, int64_t N, int64_t K, int32_t V) {
+    size_t b = round_up(static_cast<size_t>(pad16(static_cast<int>(M))) * K * 2, kAlign);
+    if (materialise(M, N, K, V)) b += round_up(static_cast<size_t>(mat_slots(M, V) * N * K * 2), kAlign);
+    return b;
 }
 
 }  // namespace
@@ -279,7 +307,7 @@ bool prefill_tc_supported(const LinearArgs& a) {
 
 size_t tc_scratch_bytes(int64_t M, int64_t N, int64_t K, int32_t V) {
     size_t a = decode_tc_scratch_bytes(M, N, K, V);
-    size_t b = (K % kBK == 0 && M >= 1) ? prefill_scratch_bytes(M, K) : 0;
+    size_t b = (K % kBK == 0 && M >= 1 && M <= 65520) ? prefill_scratch_bytes(M, N, K, V) : 0;
     size_t c = decode_fold_scratch_bytes(M, N, K, V);
     size_t m = a > b ? a : b;
     return m > c ? m : c;
@@ -306,8 +334,12 @@ bd_path choose_path(const LinearArgs& a) {
 bd_status launch_prefill_tc(const LinearArgs& a, const LinearWorkspace& w, cudaStream_t s) {
     const int M = static_cast<int>(a.M), N = static_cast<int>(a.N), K = static_cast<int>(a.K);
     const int Mpad = pad16(M);
-    if (prefill_scratch_bytes(a.M, a.K) > w.tc_bytes) return BD_ERR_WORKSPACE;
+    if (prefill_scratch_bytes(a.M, a.N, a.K, a.V) > w.tc_bytes) return BD_ERR_WORKSPACE;
     uint16_t* xg = static_cast<uint16_t*>(w.tc_scratch);
+    const bool mat = materialise(a.M, a.N, a.K, a.V);
+    uint8_t* weff = static_cast<uint8_t*>(w.tc_scratch) +
+                    round_up(static_cast<size_t>(Mpad) * a.K * 2, kAlign);
+    if (mat && launch_reconstruct_plan(a, w.g.plan, weff, s) != BD_OK) return BD_ERR_CUDA;
     gather_x_kernel<<<dim3((K / 8 + 255) / 256 < 8 ? (K / 8 + 255) / 256 : 8, Mpad), 256, 0, s>>>(
         static_cast<const uint4*>(a.x), K, w.g.plan, w.g.pos2tok, reinterpret_cast<uint4*>(xg));
     if (launch_status() != BD_OK) return BD_ERR_CUDA;
@@ -316,6 +348,10 @@ bd_status launch_prefill_tc(const LinearArgs& a, const LinearWorkspace& w, cudaS
     PrefillParams p;
     memset(&p, 0, sizeof p);
     static_assert(kBN <= 256 && kBX <= 256, "TMA boxes are at most 256 rows");
+    p.prebuilt = mat ? 1 : 0;
+    if (mat)
+        for (int64_t d = 0; d < mat_slots(a.M, a.V); ++d)
+            if (!make_tmap_bf16_sw128(&p.tm_weff[d], weff + d * a.N * a.K * 2, a.N, a.K, kBN)) return BD_ERR_CUDA;
     if (!make_tmap_bf16_sw128(&p.tm_w, a.w_base, a.N, a.K, kBN) ||
         !make_tmap_bf16_sw128(&p.tm_x, xg, Mpad, a.K, kBX))
         return BD_ERR_CUDA;

@@ -4,9 +4,11 @@
 // "Serving architecture" (the conceptual listing rebuilds
 // W_eff = W_base + alpha * sign(delta) in the base dtype and hands it to a
 // standard linear) and section "Latency profile" (reconstruction in prefill,
-// then the standard matmul path).  The fused kernels never write W_eff; this
-// kernel does, once per variant, so that "reconstruct, then a library GEMM"
-// can be run and timed beside the fused path.
+// then the standard matmul path).  The decode kernels never write W_eff.
+// This file writes it once per variant: for callers (bitdelta_reconstruct,
+// e.g. to run "reconstruct, then a library GEMM" beside the fused path) and
+// for the prefill path, which materialises every present variant of a large
+// batch and then multiplies without rebuilding W tiles in shared memory.
 //
 // W_eff[n,k] = bf16_rne(W_base[n,k] + a s[n,k]), a = alpha (one per matrix)
 // or alpha[n] (one per output row), s = +1 for a stored 1 bit, -1 for a 0.
@@ -19,6 +21,7 @@
 // weight.  Each thread handles 8 consecutive weights (one 16-byte load and
 // store, one byte of bits); the grid strides over the matrix.
 #include "bd_internal.cuh"
+#include "bd_paths.cuh"
 
 namespace bd {
 namespace {
@@ -77,7 +80,49 @@ __global__ void __launch_bounds__(kThreads) reconstruct_kernel(const uint4* __re
     }
 }
 
+// Every variant present in a grouped batch (slot d of the segment plan):
+// W_eff of variant plan->var[d] into weff + d * N * K.  Used by the prefill
+// path, which then multiplies the tokens of slot d with it.
+__global__ void __launch_bounds__(kThreads) reconstruct_plan_kernel(const uint4* __restrict__ w_base,
+                                                                    BitsTable bt, const float* __restrict__ alphas,
+                                                                    int alpha_rows, const SegPlan* __restrict__ plan,
+                                                                    int64_t N, int64_t K, uint4* __restrict__ weff) {
+    const int64_t chunks = N * K / 8, per_row = K / 8;
+    const int D = plan->D;
+    for (int d = 0; d < D; ++d) {
+        const int v = plan->var[d];
+        const uint8_t* bits = bt.p[v];
+        uint4* out = weff + static_cast<int64_t>(d) * chunks;
+        const float a0 = alpha_rows ? 0.f : __ldg(alphas + v);
+        for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < chunks;
+             c += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+            const float a = alpha_rows ? __ldg(alphas + static_cast<int64_t>(v) * N + c / per_row) : a0;
+            const uint4 w = __ldg(w_base + c);
+            const uint32_t b = __ldg(bits + c);
+            uint4 o;
+            o.x = eff_pair(w.x, b, a);
+            o.y = eff_pair(w.y, b >> 2, a);
+            o.z = eff_pair(w.z, b >> 4, a);
+            o.w = eff_pair(w.w, b >> 6, a);
+            out[c] = o;
+        }
+    }
+}
+
 }  // namespace
+
+bd_status launch_reconstruct_plan(const LinearArgs& a, const SegPlan* plan, void* weff, cudaStream_t s) {
+    const int64_t chunks = a.N * a.K / 8;
+    int sms = sm_count();
+    int64_t blocks = (chunks + kThreads - 1) / kThreads;
+    const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 1) * 16;
+    if (blocks > cap) blocks = cap;
+    reconstruct_plan_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(
+        static_cast<const uint4*>(a.w_base), a.bits, a.alphas, a.alpha_rows, plan, a.N, a.K,
+        static_cast<uint4*>(weff));
+    return launch_status();
+}
+
 }  // namespace bd
 
 using namespace bd;

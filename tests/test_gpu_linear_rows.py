@@ -107,3 +107,39 @@ def test_rows_constant_equals_per_matrix(bd):
         y1 = bd.linear(x, ids, wb, alphas, bits, path=path)
         y2 = bd.linear_rows(x, ids, wb, arows, bits, path=path)
         assert torch.equal(y1, y2), path
+
+
+@pytest.mark.parametrize("per_row", [False, True])
+def test_prefill_materialised(bd, o, per_row):
+    """Prefill with >= 2048 tokens per variant: each present variant's W_eff is
+    materialised once (nearest bf16) and multiplied without the in-tile
+    rewrite; ragged N, base-model tokens mixed in, 64 sampled rows."""
+    g = wl.generator(150 + int(per_row), DEV)
+    N, K, V, per = 1000, 1024, 2, 2304
+    wb = wl.base_weights(N, K, g, DEV)
+    bits, alphas, arows = [], [], []
+    for _ in range(V):
+        wf = wl.finetuned_weights(wb, 8e-4, g)
+        if per_row:
+            a, b = bd.compress_rows(wf, wb)
+            arows.append(a)
+        else:
+            a, b = bd.compress(wf, wb)
+            alphas.append(a)
+        bits.append(b)
+    ids = torch.cat([torch.full((per,), v, dtype=torch.int32, device=DEV) for v in range(V)] +
+                    [torch.full((100,), -1, dtype=torch.int32, device=DEV)])
+    ids = ids[torch.randperm(ids.numel(), generator=torch.Generator().manual_seed(151)).to(DEV)]
+    x = wl.activations(ids.numel(), K, g, DEV)
+    rows = np.sort(np.random.default_rng(152).choice(N, 64, replace=False))
+    if per_row:
+        al = torch.stack(arows).contiguous()
+        y = bd.linear_rows(x, ids, wb, al, bits, path="prefill_tc").float().cpu().numpy()
+        ref = o.linear(bf16_np(x), ids.cpu().numpy(), bf16_np(wb), f32_np(al), [bits_np(b) for b in bits],
+                       rows=rows, per_row_alpha=True)
+    else:
+        al = torch.cat(alphas)
+        y = bd.linear(x, ids, wb, al, bits, path="prefill_tc").float().cpu().numpy()
+        ref = o.linear(bf16_np(x), ids.cpu().numpy(), bf16_np(wb), f32_np(al), [bits_np(b) for b in bits],
+                       rows=rows)
+    assert_y_close(y.astype(np.float64)[:, rows], ref, "prefill materialised per_row=%s" % per_row)
