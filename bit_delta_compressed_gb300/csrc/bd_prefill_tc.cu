@@ -224,7 +224,36 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_built[s]);
         }
-        if (ok && mbar_wait_sleep(&acc_full, 0, kWaitLimit, p.status, 14, p.diag)) {
+        const bool acc_ok = ok && mbar_wait_sleep(&acc_full, 0, kWaitLimit, p.status, 14, p.diag);
+        if (acc_ok && p.y_bf16 && p.N % 8 == 0) {
+            // bf16 outputs: stage the tile as [token][row] in the (now idle)
+            // pipeline memory, then write each token's kBN outputs as one
+            // contiguous 16-byte-per-lane row of y
+            tc_fence_after();
+            const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
+            const int ntok = min(kBT, pos_end - pos0);
+            __nv_bfloat16* tile = reinterpret_cast<__nv_bfloat16*>(base);
+            for (int c0 = 0; c0 < ntok; c0 += 16) {
+                uint32_t v[16];
+                const int col = kBX * (rt * kTokTiles + c0 / kBX) + c0 % kBX;
+                tmem_ld16(tmem + lane_addr + col, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) tile[(c0 + i) * kBN + r] = __float2bfloat16_rn(__uint_as_float(v[i]));
+            }
+            asm volatile("bar.sync 1, %0;" ::"r"(kBuildWarps * 32) : "memory");
+            const int rows = min(kBN, p.N - n0);
+            for (int t = warp - 2; t < ntok; t += kBuildWarps) {
+                __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.y) + static_cast<int64_t>(p.pos2tok[pos0 + t]) * p.N + n0;
+                const __nv_bfloat16* src = tile + t * kBN;
+                if (rows == kBN) {
+                    static_assert(kBN == 32 * 8, "one 16-byte vector per lane per token row");
+                    reinterpret_cast<uint4*>(dst)[lane] = reinterpret_cast<const uint4*>(src)[lane];
+                } else {
+                    for (int rr = lane; rr < rows; rr += 32) dst[rr] = src[rr];
+                }
+            }
+        } else if (acc_ok) {
             tc_fence_after();
             const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
             for (int c0 = 0; c0 < kBT && pos0 + c0 < pos_end; c0 += 16) {
