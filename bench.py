@@ -76,8 +76,10 @@ def peaks():
 
 KERNEL_SOURCES = {
     "compress_28672x8192": ["bd_compress.cu", "bd_internal.cuh"],
+    # the decode step's kernels (grouping, staging, the shared-accumulator linear), its
+    # dispatch and the helpers they are built from
     "linear_stack70b": ["bd_linear.cu", "bd_paths.cuh", "bd_internal.cuh", "bd_decode_tc.cu",
-                        "bd_decode_fold.cu", "bd_prefill_tc.cu", "bd_tc_common.cuh", "bd_sm100.cuh"],
+                        "bd_decode_fold.cu", "bd_tc_common.cuh", "bd_sm100.cuh"],
 }
 
 

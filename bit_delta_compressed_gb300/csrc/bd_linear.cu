@@ -609,6 +609,28 @@ bd_status prepare(const void* x, int64_t M, int64_t N, int64_t K, const void* w_
     return BD_OK;
 }
 
+}  // namespace
+
+bd_path choose_path(const LinearArgs& a) {
+    // GEMV (CUDA cores) for 1-2 tokens; from 3 tokens the tensor-core decode
+    // kernel is faster (4096 x 4096: 11.9 / 14.5 / 24.6 / 26.6 us for 1-4
+    // tokens on CUDA cores against 22.5 us on tensor cores)
+    if (a.M <= 2) return BD_PATH_SIMT;
+    // Measured on GB300 (q, k/v, gate and 4096 x 4096 shapes, 2 to 14 Zipf
+    // variants, 16 to 128 tokens): the per-variant sign kernel wins for few
+    // variants or few tokens; the folded kernel, whose cost hardly grows with
+    // the number of variants, wins from 32 tokens on once there are 8 or more
+    // variants, and from 32 tokens on for narrow outputs (N <= 2048) whatever
+    // the variant count.
+    if (a.V >= 2 && a.M >= 32 && (a.V >= 8 || a.N <= 2048) && decode_fold_supported(a))
+        return BD_PATH_DECODE_FOLD;
+    if (decode_tc_supported(a)) return BD_PATH_DECODE_TC;
+    if (prefill_tc_supported(a)) return BD_PATH_PREFILL_TC;
+    return BD_PATH_SIMT;
+}
+
+namespace {
+
 bd_status launch_path(bd_path path, const LinearArgs& a, const LinearWorkspace& w,
                       cudaStream_t s) {
     switch (path) {

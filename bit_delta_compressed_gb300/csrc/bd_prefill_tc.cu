@@ -1,5 +1,5 @@
 // bd_prefill_tc.cu -- tensor-core prefill path of the fused multi-variant
-// linear, and the choice of path.
+// linear.
 //
 // Page: "BitDelta: serving 14 Zen models from one GPU cluster", section
 // "Serving architecture" (reconstruction W_eff = W_base + alpha_v *
@@ -340,24 +340,6 @@ size_t tc_scratch_bytes(int64_t M, int64_t N, int64_t K, int32_t V) {
     size_t c = decode_fold_scratch_bytes(M, N, K, V);
     size_t m = a > b ? a : b;
     return m > c ? m : c;
-}
-
-bd_path choose_path(const LinearArgs& a) {
-    // GEMV (CUDA cores) for 1-2 tokens; from 3 tokens the tensor-core decode
-    // kernel is faster (4096 x 4096: 11.9 / 14.5 / 24.6 / 26.6 us for 1-4
-    // tokens on CUDA cores against 22.5 us on tensor cores)
-    if (a.M <= 2) return BD_PATH_SIMT;
-    // Measured on GB300 (q, k/v, gate and 4096 x 4096 shapes, 2 to 14 Zipf
-    // variants, 16 to 128 tokens): the per-variant sign kernel wins for few
-    // variants or few tokens; the folded kernel, whose cost hardly grows with
-    // the number of variants, wins from 32 tokens on once there are 8 or more
-    // variants, and from 32 tokens on for narrow outputs (N <= 2048) whatever
-    // the variant count.
-    if (a.V >= 2 && a.M >= 32 && (a.V >= 8 || a.N <= 2048) && decode_fold_supported(a))
-        return BD_PATH_DECODE_FOLD;
-    if (decode_tc_supported(a)) return BD_PATH_DECODE_TC;
-    if (prefill_tc_supported(a)) return BD_PATH_PREFILL_TC;
-    return BD_PATH_SIMT;
 }
 
 bd_status launch_prefill_tc(const LinearArgs& a, const LinearWorkspace& w, cudaStream_t s) {
