@@ -611,6 +611,7 @@ bd_status prepare(const void* x, int64_t M, int64_t N, int64_t K, const void* w_
 
 }  // namespace
 
+namespace bd {
 bd_path choose_path(const LinearArgs& a) {
     // GEMV (CUDA cores) for 1-2 tokens; from 3 tokens the tensor-core decode
     // kernel is faster (4096 x 4096: 11.9 / 14.5 / 24.6 / 26.6 us for 1-4
@@ -628,6 +629,8 @@ bd_path choose_path(const LinearArgs& a) {
     if (prefill_tc_supported(a)) return BD_PATH_PREFILL_TC;
     return BD_PATH_SIMT;
 }
+
+}  // namespace bd
 
 namespace {
 
