@@ -14,8 +14,10 @@ independent replica; the path has no data exchange).
 
 The same run also times, on rank 0, the other steps of the path on their own
 workloads ("rows"): compression of 14 variants of a 28672 x 8192 matrix, the
-prefill linear (gate and up, 4 variants x 4096 tokens), and the single
-4096 x 4096 linear at 1..64 tokens.
+prefill linear (gate and up, 4 variants x 4096 tokens), the single
+4096 x 4096 linear at 1..64 tokens, the 14-variant FFN up-projection
+(14336 x 4096, 64 tokens), per-row scales, the materialised reconstruction
+and the delta cache.
 
 ``--impl reference`` times the CPU oracle on a bounded sample of the same
 workload instead (host cores only).
@@ -54,7 +56,7 @@ def parse_args():
     p.add_argument("--variants", type=int, default=14)
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-rows", action="store_true", help="skip the compress/prefill/single rows")
-    p.add_argument("--only", choices=["compress", "prefill", "single", "alpha_rows", "reconstruct", "delta_cache"],
+    p.add_argument("--only", choices=["compress", "prefill", "single", "ffn14", "alpha_rows", "reconstruct", "delta_cache"],
                    default=None,
                    help="run just one row (for profiling); prints only that row")
     p.add_argument("--compress-variants", type=int, default=14)
@@ -78,8 +80,8 @@ KERNEL_SOURCES = {
     "compress_28672x8192": ["bd_compress.cu", "bd_internal.cuh"],
     # the decode step's kernels (grouping, staging, the shared-accumulator linear), its
     # dispatch and the helpers they are built from
-    "linear_stack70b": ["bd_linear.cu", "bd_paths.cuh", "bd_internal.cuh", "bd_decode_tc.cu",
-                        "bd_decode_fold.cu", "bd_tc_common.cuh", "bd_sm100.cuh"],
+    "linear_stack70b": ["bd_linear.cu", "bd_paths.cuh", "bd_internal.cuh", "bd_decode_fold.cu",
+                        "bd_tmap.cu", "bd_tc_common.cuh", "bd_sm100.cuh"],
 }
 
 
@@ -453,6 +455,24 @@ def measure_chained(args, torch, bd, linears, ids, ws, V, stream):
                         "gate, up <- h1; down <- silu(gate) * up; h2 = h1 + down (glue in torch)"}
 
 
+def time_graph(torch, fn, iters, stream):
+    """Time per replay of ``fn`` captured in a CUDA graph: the same launches
+    without the per-call host work.  Returns (ms, None), or (None, reason)
+    when capture fails."""
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            fn()
+    except Exception as e:          # reported in the row; the eager figures stand
+        torch.cuda.synchronize()
+        return None, "%s: %s" % (type(e).__name__, str(e).splitlines()[0] if str(e) else "")
+    graph.replay()
+    torch.cuda.synchronize()
+    ms = time_events(torch, graph.replay, iters, stream)
+    del graph
+    return ms, None
+
+
 def time_events(torch, fn, iters, stream):
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
@@ -465,7 +485,7 @@ def time_events(torch, fn, iters, stream):
 
 
 def run_rows(args, torch, bd, wl, dev, pk,
-             which=("compress", "prefill", "single", "alpha_rows", "reconstruct", "delta_cache")):
+             which=("compress", "prefill", "single", "ffn14", "alpha_rows", "reconstruct", "delta_cache")):
     """Compress, prefill, the single-linear decode, the per-row-scale linear
     and the materialised reconstruction on their own workloads."""
     rows = {}
@@ -478,6 +498,9 @@ def run_rows(args, torch, bd, wl, dev, pk,
         torch.cuda.empty_cache()
     if "single" in which:
         rows["single4096"] = row_single(args, torch, bd, wl, dev, pk, g)
+        torch.cuda.empty_cache()
+    if "ffn14" in which:
+        rows["ffn14"] = row_ffn14(args, torch, bd, wl, dev, pk, g)
         torch.cuda.empty_cache()
     if "alpha_rows" in which:
         rows["alpha_rows"] = row_alpha_rows(args, torch, bd, wl, dev, pk, g)
@@ -567,7 +590,10 @@ def row_prefill(args, torch, bd, wl, dev, pk, g):
 
 def row_single(args, torch, bd, wl, dev, pk, g):
     """Single 4096 x 4096 linear, 1 variant, M in {1, 8, 32, 64}; 16 weight
-    copies rotate so that every call reads from HBM (> 2x L2)."""
+    copies rotate so that every call reads from HBM (> 2x L2).  Timed twice:
+    eager calls (host work per call included: at these sizes the host can
+    take longer than the device) and the same calls replayed from a CUDA
+    graph (device time; the roofline fraction of the launches)."""
     stream = torch.cuda.current_stream()
     N = K = 4096
     copies = 16
@@ -592,9 +618,57 @@ def row_single(args, torch, bd, wl, dev, pk, g):
         run_all()
         ms = time_events(torch, run_all, 10, stream) / copies
         byt = linear_bytes(M, N, K, 1)
-        ach = byt / (ms / 1e3) / 1e9
-        single["M=%d" % M] = {"us": ms * 1e3, "achieved_gbs": ach, "frac": ach / pk["hbm_gbs"]}
+        single["M=%d" % M] = launch_figures(torch, run_all, ms, copies, byt, pk, stream)
     return single
+
+
+def launch_figures(torch, fn, eager_ms, calls, byt, pk, stream):
+    """Eager and graph-replayed time per call of ``fn`` (``calls`` linears),
+    with the achieved bandwidth of each."""
+    out = {"eager_us": eager_ms * 1e3, "eager_gbs": byt / (eager_ms / 1e3) / 1e9}
+    out["eager_frac"] = out["eager_gbs"] / pk["hbm_gbs"]
+    gms, err = time_graph(torch, fn, 10, stream)
+    if gms is None:
+        out["graph"] = "capture failed: " + err
+        return out
+    gms /= calls
+    out["graph_us"] = gms * 1e3
+    out["graph_gbs"] = byt / (gms / 1e3) / 1e9
+    out["graph_frac"] = out["graph_gbs"] / pk["hbm_gbs"]
+    return out
+
+
+def row_ffn14(args, torch, bd, wl, dev, pk, g):
+    """Multi-tenant FFN up-projection 14336 x 4096, 14 variants (Laplace
+    scales uniform in [2e-4, 2e-3]), 64 tokens with uniform ids, through the
+    automatic path; 3 weight sets rotate (> 4x L2)."""
+    stream = torch.cuda.current_stream()
+    N, K, V, M = 14336, 4096, 14, 64
+    sets = 3
+    alphas = torch.tensor(wl.scales_uniform(V, 2e-4, 2e-3, wl.generator(args.seed + 21)),
+                          dtype=torch.float32, device=dev)
+    ids = wl.variant_ids_uniform(M, V, wl.generator(args.seed + 22)).to(dev)
+    D = int(torch.unique(ids[ids >= 0]).numel())
+    mats = []
+    for _ in range(sets):
+        w = wl.base_weights(N, K, g, dev)
+        b = [torch.randint(-2 ** 31, 2 ** 31, (N, K // 32), generator=g, device=dev,
+                           dtype=torch.int64).to(torch.int32) for _ in range(V)]
+        mats.append((w, b, bd.bits_pointer_array(b)))
+    x = wl.activations(M, K, g, dev)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    ws = bd.linear_workspace(M, N, K, V, dev)
+    bd.group(ids, V, ws)
+
+    def run_all():
+        for w, b, p in mats:
+            bd.linear_grouped(x, w, alphas, p, V, y, ws, path=args.path)
+    run_all()
+    ms = time_events(torch, run_all, 10, stream) / sets
+    out = {"shape": [N, K], "variants": V, "tokens": M, "distinct": D,
+           "algorithmic_bytes": linear_bytes(M, N, K, D)}
+    out.update(launch_figures(torch, run_all, ms, sets, out["algorithmic_bytes"], pk, stream))
+    return out
 
 
 def row_alpha_rows(args, torch, bd, wl, dev, pk, g):

@@ -31,8 +31,6 @@
 // same K slice; those passes reload only X_p and bits, never W_base.
 #include <cuda_fp8.h>
 
-#include <mutex>
-
 #include "bd_sm100.cuh"
 #include "bd_tc_common.cuh"
 
@@ -411,14 +409,47 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         if (last_cta) {
             __threadfence();
             const int rows = min(kBN, p.N - n0);
-            for (int idx = threadIdx.x; idx < p.M * rows; idx += blockDim.x) {
-                const int t = idx / rows, rr = idx % rows;
-                float acc = 0.f;
-                for (int s = 0; s < p.splits; ++s)
-                    acc += __ldcg(p.part + (static_cast<int64_t>(s) * p.M + t) * p.N + n0 + rr);
-                const int64_t o = static_cast<int64_t>(t) * p.N + n0 + rr;
-                if (p.y_bf16) static_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(acc);
-                else static_cast<float*>(p.y)[o] = acc;
+            if (rows == kBN && (p.N & 3) == 0) {
+                // four outputs per thread, slices summed in order 0, 1, 2, ...
+                // with four loads in flight
+                const int nq = kBN / 4;
+                const int64_t sq = static_cast<int64_t>(p.M) * p.N / 4;      // float4s per slice
+                for (int idx = threadIdx.x; idx < p.M * nq; idx += blockDim.x) {
+                    const int t = idx / nq, c4 = idx % nq;
+                    const float4* src = reinterpret_cast<const float4*>(p.part + static_cast<int64_t>(t) * p.N + n0) + c4;
+                    float4 acc = __ldcg(src);
+                    int sl = 1;
+                    for (; sl + 3 < p.splits; sl += 4) {
+                        const float4 a0 = __ldcg(src + sl * sq), a1 = __ldcg(src + (sl + 1) * sq);
+                        const float4 a2 = __ldcg(src + (sl + 2) * sq), a3 = __ldcg(src + (sl + 3) * sq);
+                        acc.x = (((acc.x + a0.x) + a1.x) + a2.x) + a3.x;
+                        acc.y = (((acc.y + a0.y) + a1.y) + a2.y) + a3.y;
+                        acc.z = (((acc.z + a0.z) + a1.z) + a2.z) + a3.z;
+                        acc.w = (((acc.w + a0.w) + a1.w) + a2.w) + a3.w;
+                    }
+                    for (; sl < p.splits; ++sl) {
+                        const float4 a0 = __ldcg(src + sl * sq);
+                        acc.x += a0.x; acc.y += a0.y; acc.z += a0.z; acc.w += a0.w;
+                    }
+                    const int64_t o = static_cast<int64_t>(t) * p.N + n0 + 4 * c4;
+                    if (p.y_bf16) {
+                        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+                        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.y) + o) =
+                            make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+                    } else {
+                        *reinterpret_cast<float4*>(static_cast<float*>(p.y) + o) = acc;
+                    }
+                }
+            } else {
+                for (int idx = threadIdx.x; idx < p.M * rows; idx += blockDim.x) {
+                    const int t = idx / rows, rr = idx % rows;
+                    float acc = 0.f;
+                    for (int s = 0; s < p.splits; ++s)
+                        acc += __ldcg(p.part + (static_cast<int64_t>(s) * p.M + t) * p.N + n0 + rr);
+                    const int64_t o = static_cast<int64_t>(t) * p.N + n0 + rr;
+                    if (p.y_bf16) static_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(acc);
+                    else static_cast<float*>(p.y)[o] = acc;
+                }
             }
             if (threadIdx.x == 0) p.tickets[tile] = 0u;
         }
@@ -664,75 +695,6 @@ bd_status launch_decode_tc(const LinearArgs& a, const LinearWorkspace& w, cudaSt
     cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, decode_tc_kernel, p) != cudaSuccess) return BD_ERR_CUDA;
     return launch_status();
-}
-
-// ---------------------------------------------------------------------------
-// host helpers shared with the prefill path
-// ---------------------------------------------------------------------------
-namespace {
-std::mutex g_tc_mutex;
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-int g_smem_set[64][4] = {};
-
-bool encoder() {
-    std::lock_guard<std::mutex> lock(g_tc_mutex);
-    if (!g_encode) {
-        cudaDriverEntryPointQueryResult q;
-        void* fn = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess || !fn)
-            return false;
-        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
-    return true;
-}
-}  // namespace
-
-bool make_tmap_bf16_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                          uint32_t box_rows) {
-    if (!encoder()) return false;
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 2};
-    cuuint32_t box[2] = {64, box_rows};
-    cuuint32_t es[2] = {1, 1};
-    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                    es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-bool make_tmap_u8_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols_bytes,
-                        uint32_t box_rows) {
-    if (!encoder()) return false;
-    cuuint64_t dims[2] = {cols_bytes, rows};
-    cuuint64_t strides[1] = {cols_bytes};
-    cuuint32_t box[2] = {128, box_rows};
-    cuuint32_t es[2] = {1, 1};
-    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-bool make_tmap_bits(CUtensorMap* map, const void* base, uint64_t rows, uint64_t words, uint32_t box_rows) {
-    if (!encoder()) return false;
-    cuuint64_t dims[2] = {words, rows};
-    cuuint64_t strides[1] = {words * 4};
-    cuuint32_t box[2] = {4, box_rows};
-    cuuint32_t es[2] = {1, 1};
-    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, es,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-bool set_smem_attr(const void* kernel, int bytes, int slot) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
-    std::lock_guard<std::mutex> lock(g_tc_mutex);
-    if (g_smem_set[dev][slot] >= bytes) return true;
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
-        return false;
-    g_smem_set[dev][slot] = bytes;
-    return true;
 }
 
 }  // namespace bd
