@@ -72,10 +72,12 @@ struct DecodeParams {
     unsigned* status;
     unsigned* diag;
     int M, N, K, Mb, budget, splits, y_bf16;
+    int cluster_reduce;                   // the K slices of a row tile form one cluster (2..8 slices, M <= 128)
 };
 
 constexpr uint32_t kBitsTile = kBN * 16;  // one variant, 128 rows x 4 words
 constexpr uint32_t kWTile = kBN * 128;    // 128 rows x 64 bf16
+static_assert(kWStages * kWTile >= 128 * kBN * 4, "the W ring holds a 128-token f32 partial tile");
 
 // Shared memory: W ring | activation ring (X_c rows then X_p rows per stage)
 // | bits ring (kMaxPassVariants tiles per stage).
@@ -99,8 +101,29 @@ __device__ __forceinline__ float exp2i(int e) {      // exact 2^e, e in [-126, 1
     return __int_as_float((127 + e) << 23);
 }
 
-__device__ __forceinline__ void store_y(const DecodeParams& p, int split, int t, int n, float v) {
-    if (p.splits > 1) {
+// Distributed shared memory of a thread-block cluster.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(saddr), "r"(rank));
+    return a;
+}
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
+    return v;
+}
+
+// Output (token t, row n = n0 + r) of this CTA: its partial tile in shared
+// memory (cluster reduction), its K slice's partial in HBM (ticket
+// reduction), or y itself (one slice).
+__device__ __forceinline__ void store_y(const DecodeParams& p, float* psm, int split, int t, int n, int r, float v) {
+    if (p.cluster_reduce) {
+        psm[t * kBN + r] = v;
+    } else if (p.splits > 1) {
         p.part[(static_cast<int64_t>(split) * p.M + t) * p.N + n] = v;
     } else if (p.y_bf16) {
         static_cast<__nv_bfloat16*>(p.y)[static_cast<int64_t>(t) * p.N + n] = __float2bfloat16_rn(v);
@@ -142,6 +165,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Mb = p.Mb;
     const SmemLayout L = smem_layout(Mb, p.budget);
+    // cluster reduction: the partial tile [M][128] f32 lives in the W ring,
+    // which no load or MMA touches after pass 0's MMAs have completed
+    float* psm = reinterpret_cast<float*>(base + L.w);
     const int tile = blockIdx.x / p.splits, split = blockIdx.x % p.splits;
     const int n0 = tile * kBN;
     const int kb_total = p.K / kBK;
@@ -365,10 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                     if (row_ok)
 #pragma unroll
                         for (int t = 0; t < 8; ++t)
-                            if (pos0 + t < pl.n_base) store_y(p, split, tok_s[pos0 + t], n, __uint_as_float(b[t]));
+                            if (pos0 + t < pl.n_base) store_y(p, psm, split, tok_s[pos0 + t], n, r, __uint_as_float(b[t]));
                 }
                 if (row_ok && h == 0)                                          // invalid ids: zero rows
-                    for (int pos = p.M - pl.n_invalid; pos < p.M; ++pos) store_y(p, split, tok_s[pos], n, 0.f);
+                    for (int pos = p.M - pl.n_invalid; pos < p.M; ++pos) store_y(p, psm, split, tok_s[pos], n, r, 0.f);
             }
             for (int d = q.d0; d < q.d1; ++d) {
                 const int cnt = pl.cnt[d], off = pl.off[d];
@@ -385,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
 #pragma unroll
                         for (int t = 0; t < 8; ++t) {
                             if (8 * ci + t >= cnt) break;
-                            store_y(p, split, tok_s[pos0 + t], n,
+                            store_y(p, psm, split, tok_s[pos0 + t], n, r,
                                     fmaf(ar * scale_s[pos0 + t], __uint_as_float(sg[t]), __uint_as_float(bs[t])));
                         }
                     }
@@ -398,7 +424,45 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     }
 
     __syncthreads();
-    if (p.splits > 1) {
+    if (p.cluster_reduce) {
+        // the K slices of this row tile are the CTAs of one cluster (rank =
+        // split): CTA `split` sums its share of the tile over the slices'
+        // shared memory in the order 0, 1, 2, ... and writes y
+        cluster_sync_all();
+        const int rows = min(kBN, p.N - n0);
+        const uint32_t psm_a = smem_u32(psm);
+        const int per_t = kBN / 4;                              // float4 groups per token
+        const int total = p.M * per_t;
+        const int g0 = static_cast<int>(static_cast<int64_t>(split) * total / p.splits);
+        const int g1 = static_cast<int>(static_cast<int64_t>(split + 1) * total / p.splits);
+        for (int gi = g0 + static_cast<int>(threadIdx.x); gi < g1; gi += blockDim.x) {
+            const int t = gi / per_t, r4 = 4 * (gi % per_t);
+            if (r4 >= rows) continue;
+            const uint32_t off = psm_a + static_cast<uint32_t>(gi) * 16u;
+            float4 acc = ld_cluster_f4(cluster_map(off, 0));
+            for (int sl = 1; sl < p.splits; ++sl) {
+                const float4 a = ld_cluster_f4(cluster_map(off, static_cast<uint32_t>(sl)));
+                acc.x += a.x; acc.y += a.y; acc.z += a.z; acc.w += a.w;
+            }
+            const int64_t o = static_cast<int64_t>(t) * p.N + n0 + r4;
+            if (r4 + 4 <= rows && (p.N & 3) == 0) {
+                if (p.y_bf16) {
+                    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+                    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.y) + o) =
+                        make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+                } else {
+                    *reinterpret_cast<float4*>(static_cast<float*>(p.y) + o) = acc;
+                }
+            } else {
+                const float v4[4] = {acc.x, acc.y, acc.z, acc.w};
+                for (int j = 0; j < 4 && r4 + j < rows; ++j) {
+                    if (p.y_bf16) static_cast<__nv_bfloat16*>(p.y)[o + j] = __float2bfloat16_rn(v4[j]);
+                    else static_cast<float*>(p.y)[o + j] = v4[j];
+                }
+            }
+        }
+        cluster_sync_all();            // no CTA leaves while its tile is being read
+    } else if (p.splits > 1) {
         // deterministic split-K reduction by the CTA that finishes the tile last
         if (threadIdx.x == 0) {
             __threadfence();
@@ -679,6 +743,8 @@ bd_status launch_decode_tc(const LinearArgs& a, const LinearWorkspace& w, cudaSt
     p.budget = budget;
     p.splits = splits;
     p.y_bf16 = (a.y_dtype == BD_BF16);
+    // the partial tile must fit the W ring: M <= 128 (128 x 128 f32 = 4 W tiles)
+    p.cluster_reduce = (splits > 1 && splits <= 8 && M <= 128) ? 1 : 0;
     const SmemLayout L = smem_layout(Mb, budget);
     const int smem = static_cast<int>(L.total) + 1024;
     if (!set_smem_attr(reinterpret_cast<const void*>(decode_tc_kernel), smem, 0)) return BD_ERR_CUDA;
@@ -688,11 +754,15 @@ bd_status launch_decode_tc(const LinearArgs& a, const LinearWorkspace& w, cudaSt
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(splits);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = p.cluster_reduce ? 2 : 1;
     if (cudaLaunchKernelEx(&cfg, decode_tc_kernel, p) != cudaSuccess) return BD_ERR_CUDA;
     return launch_status();
 }
