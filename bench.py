@@ -219,9 +219,10 @@ def linear_bytes(M, N, K, D, y_bytes=2):
 
 # -- CPU oracle sample -------------------------------------------------------------
 
-def oracle_sample_time(args, wl, rows_per_linear, seed):
+def oracle_sample_time(args, wl, rows_per_linear, seed, nthreads=None):
     """Time the oracle on one layer's seven linears, ``rows_per_linear`` output
-    rows each, all tokens; returns (seconds, weights covered, threads)."""
+    rows each, all tokens, on ``nthreads`` host threads (default: all);
+    returns (seconds, weights covered, threads)."""
     import numpy as np
     import torch
     import oracle
@@ -240,9 +241,9 @@ def oracle_sample_time(args, wl, rows_per_linear, seed):
         cases.append((x, wb, alphas, bits, r * K))
     t0 = time.perf_counter()
     for x, wb, alphas, bits, _ in cases:
-        o.linear(x, ids, wb, alphas, bits)
+        o.linear(x, ids, wb, alphas, bits, nthreads=nthreads)
     dt = time.perf_counter() - t0
-    return dt, sum(c[4] for c in cases), oracle.host_threads()
+    return dt, sum(c[4] for c in cases), oracle.host_threads() if nthreads is None else int(nthreads)
 
 
 def cpu_value(args, wl, seconds, weights_done):
@@ -380,6 +381,11 @@ def run_ours(args, rank, world, local_rank):
             "sample": "fp64 oracle linear on one layer's seven linears, %d output rows each, all %d "
                       "tokens, 14 variants (%.1f s); extrapolated by weight count to %d layers"
                       % (args.cpu_sample_rows, M, dt, args.layers)}
+        st_rows = max(8, args.cpu_sample_rows // 16)
+        dt1, w1, _ = oracle_sample_time(args, wl, st_rows, args.seed, nthreads=1)
+        line["cpu_baseline"]["single_thread"] = {
+            "value": cpu_value(args, wl, dt1, w1), "unit": UNIT, "cores": 1,
+            "sample": "the same, %d output rows per linear (%.1f s)" % (st_rows, dt1)}
     del linears
     torch.cuda.empty_cache()
     if rank == 0 and not args.no_rows:
