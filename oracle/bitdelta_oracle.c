@@ -19,7 +19,7 @@
  *                                      (a 4096 x 4096 weight packs to
  *                                      4096 x 512 bytes), alpha kept as f32.
  *
- * Readings where the page is silent (each one is listed in the design doc):
+ * Readings where the page is silent:
  *   - sign(0) is +1, stored as bit 1; -0 also gives bit 1.
  *   - bit order: row-major [N, K/32] little-endian u32 words, bit j of word w
  *     in row n <-> column 32*w + j (LSB first).  Byte-for-byte this is the
