@@ -70,7 +70,9 @@ typedef enum { BD_F32 = 0, BD_BF16 = 1 } bd_dtype;
 typedef enum {
     BD_PATH_AUTO = 0,
     BD_PATH_SIMT = 1,       /* CUDA-core kernel, any M */
-    BD_PATH_DECODE_TC = 2,  /* tcgen05 decode kernel: base and sign products on tensor cores */
+    BD_PATH_DECODE_TC = 2,  /* tcgen05 decode kernel: base and sign products on tensor cores;
+                               M <= 176 tokens.  With 2 to 8 K slices and M <= 128 the slices
+                               of a 128-row tile launch as one thread-block cluster */
     BD_PATH_PREFILL_TC = 3, /* tcgen05 prefill kernel: W_eff tiles built in shared memory */
     BD_PATH_DECODE_FOLD = 4 /* tcgen05 decode kernel with one sign accumulator shared by all
                                variants (a column per token), the scales applied in the epilogue:
