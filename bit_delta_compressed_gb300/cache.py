@@ -3,8 +3,11 @@
 Page: "BitDelta: serving 14 Zen models from one GPU cluster", section
 "Infrastructure details": each variant's deltas (packed sign bits and f32
 scales) live in host storage and are loaded onto the GPU on first use; the
-GPU keeps the variants in use, evicting the least recently used weighted by
-how often each is requested.
+GPU keeps the variants in use, keeping the most requested ones resident at all
+times and sharing the rest of the space among the others by recency and
+request rate (the cache-eviction paragraph: the six variants with the most
+traffic always stay loaded, the remaining eight share what is left under
+LRU).
 
 ``DeltaCache`` holds the device copies within a byte budget:
 
@@ -15,11 +18,17 @@ how often each is requested.
   for the load (if one is in flight) before it uses them.  A variant being
   loaded is loaded once: concurrent acquires share the in-flight copy.
   Acquired variants are pinned (not evictable) until ``release``.
-* Eviction, when a load needs room: among resident, unpinned variants whose
-  copy has completed, the one with the smallest score = request rate x
-  recency weight, rate an exponentially decayed request count and recency
-  exp(-age / tau); if only in-flight ones are unpinned, the oldest copy is
-  waited for first.
+* The hot set: the ``pinned_top_k`` registered variants with the highest
+  request rate (an exponentially decayed request count, ties broken by name)
+  are never evicted.  The ranking is taken afresh at every eviction, so a
+  variant whose traffic fades drops out of the hot set and becomes evictable,
+  and one whose traffic grows joins it.  ``warm()`` loads every hot variant
+  that is not resident.
+* Eviction, when a load needs room: among resident variants that are neither
+  hot nor acquired and whose copy has completed, the one with the smallest
+  score = request rate x recency weight, recency exp(-age / tau); if only
+  in-flight ones qualify, the oldest copy is waited for first.  When nothing
+  qualifies the load raises MemoryError.
 
 Copies run on a stream of their own (host-to-device from pinned memory), so a
 load overlaps compute on the caller's stream; the device tensors are marked as
@@ -55,7 +64,7 @@ class _Stats:
 
 class DeltaCache:
     def __init__(self, capacity_bytes: int, device, half_life_s: float = 60.0, tau_s: float = 30.0,
-                 clock=time.monotonic):
+                 clock=time.monotonic, pinned_top_k: int = 6):
         import torch
         self.torch = torch
         self.capacity = int(capacity_bytes)
@@ -63,6 +72,9 @@ class DeltaCache:
         self.half_life = float(half_life_s)
         self.tau = float(tau_s)
         self.clock = clock
+        if pinned_top_k < 0:
+            raise ValueError("pinned_top_k must be >= 0")
+        self.pinned_top_k = int(pinned_top_k)
         self.host: dict[str, tuple[list, list]] = {}
         self.resident: dict[str, Resident] = {}
         self.stats: dict[str, _Stats] = {}
@@ -97,25 +109,39 @@ class DeltaCache:
         st.rate += 1.0
         st.last = now
 
+    def rate(self, name: str, now: float | None = None) -> float:
+        """Request rate: the decayed request count, decayed to ``now``."""
+        now = self.clock() if now is None else now
+        st = self.stats[name]
+        return st.rate * math.pow(0.5, max(0.0, now - st.last) / self.half_life)
+
     def score(self, name: str, now: float | None = None) -> float:
         """Request rate (decayed to ``now``) times the recency weight."""
         now = self.clock() if now is None else now
-        st = self.stats[name]
-        age = max(0.0, now - st.last)
-        rate = st.rate * math.pow(0.5, age / self.half_life)
-        return rate * math.exp(-age / self.tau)
+        age = max(0.0, now - self.stats[name].last)
+        return self.rate(name, now) * math.exp(-age / self.tau)
+
+    def hot_set(self, now: float | None = None) -> set:
+        """The ``pinned_top_k`` registered variants with the highest request
+        rate (variants never requested are not ranked)."""
+        now = self.clock() if now is None else now
+        ranked = sorted((n for n in self.stats if self.stats[n].rate > 0.0),
+                        key=lambda n: (-self.rate(n, now), n))
+        return set(ranked[:self.pinned_top_k])
 
     def _evict_for(self, need: int, now: float) -> None:
         self.poll()
+        hot = self.hot_set(now)
         while self.used + need > self.capacity:
-            cands = [r for r in self.resident.values() if r.pins == 0 and not r.loading]
+            free = [r for r in self.resident.values() if r.pins == 0 and r.name not in hot]
+            cands = [r for r in free if not r.loading]
             if not cands:
-                # unpinned variants whose copies are still in flight become
-                # evictable once their copy completes: wait for the oldest
-                waiting = [r for r in self.resident.values() if r.pins == 0 and r.loading]
+                # variants whose copies are still in flight become evictable
+                # once their copy completes: wait for the oldest
+                waiting = [r for r in free if r.loading]
                 if not waiting:
-                    raise MemoryError("delta cache: %d bytes needed, %d free and nothing evictable"
-                                      % (need, self.capacity - self.used))
+                    raise MemoryError("delta cache: %d bytes needed, %d free and nothing evictable "
+                                      "(hot set %s)" % (need, self.capacity - self.used, sorted(hot)))
                 waiting[0].ready.synchronize()
                 self.poll()
                 continue
@@ -179,6 +205,17 @@ class DeltaCache:
         self.stats[name].loads += 1
         self.bytes_loaded += need
         return r
+
+    def warm(self) -> list:
+        """Load every variant of the hot set that is not resident (without
+        counting a request); returns the names loaded."""
+        now = self.clock()
+        loaded = []
+        for name in sorted(self.hot_set(now), key=lambda n: (-self.rate(n, now), n)):
+            if name not in self.resident:
+                self._load(name, now)
+                loaded.append(name)
+        return loaded
 
     def poll(self) -> None:
         """Mark finished loads (their copies are complete) as evictable."""
