@@ -600,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1) fold_decode_kernel(const __grid_c
 //       64 of lo, byte 32w + 4j + b of a half holding column 32w + j + 8b;
 //       otherwise zeros;
 //   s_t = 7 - floor(log2(max_k |x[t,k]|)) (0 for zero rows), clamped to
-//       [-64, 64];
+//       [-120, 120];
 //   the split-K tickets zeroed.
 // ---------------------------------------------------------------------------
 // Largest |x| of a bf16 row (bf16 bit patterns without the sign order like
@@ -624,12 +624,14 @@ __device__ float row_absmax(const uint4* __restrict__ src, int64_t vec_per_row) 
 }
 
 // s with 2^s xmax in [128, 256) (0 for a zero or non-finite maximum),
-// clamped to [-64, 64].
+// clamped to [-120, 120] like the per-variant kernel's: every token whose
+// largest |x| lies in [2^-113, 2^128) gets the full range; 2^s and 2^-s stay
+// normal floats.
 __device__ __forceinline__ int scale_exponent(float xmax) {
     if (!(xmax > 0.f) || !(xmax < 3.0e38f)) return 0;
     const int biased = static_cast<int>((__float_as_uint(xmax) >> 23) & 0xFF);
-    const int e = biased > 0 ? biased - 127 : -127;
-    return max(-64, min(64, 7 - e));
+    const int e = biased > 0 ? biased - 127 : -126;
+    return max(-120, min(120, 7 - e));
 }
 
 __global__ void __launch_bounds__(256) fold_prep_kernel(const uint4* __restrict__ x, int K, int M, int Mb,
