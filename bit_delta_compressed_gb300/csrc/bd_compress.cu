@@ -16,7 +16,6 @@
 // and the last block to finish (an atomic ticket) adds the partials in a fixed
 // order and writes alpha = f32(sum / n).  Grid size depends only on the shape
 // and the device, so the result is bit-reproducible on a given device.
-#include <mutex>
 
 #include "bd_internal.cuh"
 
@@ -290,25 +289,16 @@ constexpr int kNoAllocMaxBlocks = 2048;
 constexpr size_t kNoAllocScratchBytes = kHeaderBytes + sizeof(double) * kNoAllocMaxBlocks;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kNoAllocMaxDevices = 64;
-std::mutex g_noalloc_mutex;
-void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
-
 // Device address of the static scratch on the current device.  In host code
 // the array's name stands for a host-side shadow, not device memory, so the
-// address is looked up once per device (with that device current) and cached.
+// address is looked up with the device current.  The lookup is repeated on
+// every call (it allocates nothing and costs a table lookup once the module
+// is loaded): a cached address would go stale if the primary context were
+// reset and the module reloaded elsewhere.
 bd_status noalloc_scratch(void** out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return BD_ERR_CUDA;
-    if (dev < 0 || dev >= kNoAllocMaxDevices) return BD_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (g_noalloc_ptr[dev] == nullptr) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
-            return BD_ERR_CUDA;
-        g_noalloc_ptr[dev] = p;
-    }
-    *out = g_noalloc_ptr[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return BD_ERR_CUDA;
+    *out = p;
     return BD_OK;
 }
 
@@ -323,8 +313,10 @@ extern "C" bd_status bitdelta_compress_noalloc(const void* w_ft, const void* w_b
     if (st != BD_OK) return st;
     const bool f32 = (in_dtype == BD_F32);
     const int64_t n_chunks = N * K / 8;
-    const int grid = compress_grid(n_chunks, f32);
-    if (grid > kNoAllocMaxBlocks) return BD_ERR_WORKSPACE;   // more partials than the array holds
+    // at most one fp64 partial per block fits the array; the kernel's
+    // grid-stride loop covers any matrix with fewer blocks
+    int grid = compress_grid(n_chunks, f32);
+    if (grid > kNoAllocMaxBlocks) grid = kNoAllocMaxBlocks;
     void* scratch = nullptr;
     st = noalloc_scratch(&scratch);
     if (st != BD_OK) return st;
