@@ -42,6 +42,9 @@ sys.path.insert(0, str(ROOT))
 METRIC = "BitDelta fused linear: % HBM roofline (decode), % TC peak (prefill), tok/s"
 UNIT = "tok/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# GB300's nominal HBM3e bandwidth (~8 TB/s): a second, fixed denominator beside
+# the measured copy peak
+NOMINAL_HBM_GBS = 8000.0
 
 
 def parse_args():
@@ -101,11 +104,17 @@ def profiled_traffic(kernel_key: str):
     sources: a line 'traffic <key> <bytes> sources <digest>' in profiles/*.md.
     None when absent or when the sources changed since the capture."""
     digest = sources_digest(KERNEL_SOURCES.get(kernel_key, []))
+    stale = []
     for f in sorted((ROOT / "profiles").glob("*.md")):
         for line in f.read_text().splitlines():
             m = re.match(r"\s*traffic\s+(\S+)\s+([0-9.eE+]+)\s+sources\s+(\w+)", line)
-            if m and m.group(1) == kernel_key and m.group(3) == digest:
-                return float(m.group(2))
+            if m and m.group(1) == kernel_key:
+                if m.group(3) == digest:
+                    return float(m.group(2))
+                stale.append("%s (%s)" % (f.name, m.group(3)))
+    sys.stderr.write("bench: no ncu traffic figure for %s matches the current sources (digest %s; %s); "
+                     "reporting traffic null\n" % (kernel_key, digest,
+                                                   "stale: " + ", ".join(stale) if stale else "none recorded"))
     return None
 
 
@@ -274,11 +283,17 @@ def run_reference(args, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": stack_config(args, None),
+            "data": "synthetic", "config": stack_config(args, reference_distinct(args, wl)),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def reference_distinct(args, wl):
+    """Distinct variants of rank 0's batch (the same ids the GPU arm draws)."""
+    return distinct_count(wl.variant_ids_zipf(args.tokens, args.variants, 1.1,
+                                              wl.generator(args.seed + 1)).tolist())
 
 
 def stack_config(args, D):
@@ -340,6 +355,7 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     torch.cuda.synchronize()
     t0, t1 = new_event(), new_event()
+    launches0 = int(bd.get_lib().bitdelta_launch_count())
     torch.cuda.profiler.start()       # bounds an ncu launch list to the timed region
     t0.record(stream)
     for s_i in range(args.steps):
@@ -347,6 +363,7 @@ def run_ours(args, rank, world, local_rank):
     t1.record(stream)
     torch.cuda.synchronize()
     torch.cuda.profiler.stop()
+    launches = int(bd.get_lib().bitdelta_launch_count()) - launches0
     barrier()
     clocks = sampler.stop() if sampler else None
     ms_per_step = max_over_ranks(t0.elapsed_time(t1) / args.steps, world, dev)
@@ -359,6 +376,7 @@ def run_ours(args, rank, world, local_rank):
     achieved = alg / (launch_ms / 1e3) / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
             "frac": achieved / pk["hbm_gbs"], "traffic": profiled_traffic("linear_stack70b"),
+            "nominal_peak": NOMINAL_HBM_GBS, "frac_nominal": achieved / NOMINAL_HBM_GBS,
             "kernel": "fused multi-variant linear (%s path)" % args.path,
             "alg_bytes_per_launch": alg, "avg_launch_us": launch_ms * 1e3,
             "peak_source": ("measured: MEASURED_PEAKS.json hbm_gbs (copy)" if pk_src == "measured"
@@ -372,7 +390,7 @@ def run_ours(args, rank, world, local_rank):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded; random-init 70B-shaped weights, Laplace deltas)",
             "config": stack_config(args, D), "roofline": roof, "e2e": e2e,
-            "gpu_launches": (1 + n_lin) * args.steps, "clocks": clocks, "chained": chained}
+            "gpu_launches": launches, "clocks": clocks, "chained": chained}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         dt, w_done, threads = oracle_sample_time(args, wl, args.cpu_sample_rows, args.seed)
@@ -397,37 +415,74 @@ def run_ours(args, rank, world, local_rank):
 def measure_e2e(args, torch, bd, linears, ids, ws, V, stream):
     """Same metric through the public API with host buffers: per step the
     activations and ids go host->device from pinned memory and every y comes
-    back device->host, inside the timed region."""
+    back device->host, inside the timed region.  The copies run on streams of
+    their own, as a serving loop would issue them: linear i's input copy
+    overlaps the compute of the linears before it and its output copy the
+    compute of those after it.  Events order every buffer's reuse: a step's
+    copy into x_i waits for the previous step's linear i, its linear i waits
+    for the previous step's copy out of y_i, and the ids wait for the previous
+    grouping."""
     hx = [L["x"].cpu().pin_memory() for L in linears]
     hy = [torch.empty(L["y"].shape, dtype=L["y"].dtype, pin_memory=True) for L in linears]
     hids = ids.cpu().pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in hx) + hids.numel() * 4
     d2h = sum(t.numel() * t.element_size() for t in hy)
+    n = len(linears)
+    dev = ids.device
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev = lambda: torch.cuda.Event()
+    ev_in, ev_done, ev_out = [ev() for _ in range(n)], [ev() for _ in range(n)], [ev() for _ in range(n)]
+    ev_ids, ev_group = ev(), ev()
+    state = {"first": True}
 
     def e2e_step():
-        ids.copy_(hids, non_blocking=True)
-        for L, h in zip(linears, hx):
-            L["x"].copy_(h, non_blocking=True)
+        first = state["first"]
+        with torch.cuda.stream(s_in):
+            if not first:
+                s_in.wait_event(ev_group)
+            ids.copy_(hids, non_blocking=True)
+            ev_ids.record(s_in)
+            for i, (L, h) in enumerate(zip(linears, hx)):
+                if not first:
+                    s_in.wait_event(ev_done[i])
+                L["x"].copy_(h, non_blocking=True)
+                ev_in[i].record(s_in)
+        stream.wait_event(ev_ids)
         bd.group(ids, V, ws)
-        for L in linears:
+        ev_group.record(stream)
+        for i, L in enumerate(linears):
+            stream.wait_event(ev_in[i])
+            if not first:
+                stream.wait_event(ev_out[i])
             bd.linear_grouped(L["x"], L["wb"], L["alphas"], L["ptrs"], V, L["y"], ws, path=args.path)
-        for L, h in zip(linears, hy):
-            h.copy_(L["y"], non_blocking=True)
+            ev_done[i].record(stream)
+        with torch.cuda.stream(s_out):
+            for i, (L, h) in enumerate(zip(linears, hy)):
+                s_out.wait_event(ev_done[i])
+                h.copy_(L["y"], non_blocking=True)
+                ev_out[i].record(s_out)
+        state["first"] = False
 
     for _ in range(2):
         e2e_step()
     torch.cuda.synchronize()
-    n = max(3, args.steps // 5)
+    n_steps = max(3, args.steps // 5)
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(n):
+    s_in.wait_event(a)
+    s_out.wait_event(a)
+    for _ in range(n_steps):
         e2e_step()
+    stream.wait_stream(s_in)
+    stream.wait_stream(s_out)
     b.record(stream)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / n
+    ms = a.elapsed_time(b) / n_steps
     return {"value": args.tokens / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+            "copies": "pinned host buffers; input and output copies on their own streams, "
+                      "overlapping the compute of other linears"}
 
 
 def measure_chained(args, torch, bd, linears, ids, ws, V, stream):

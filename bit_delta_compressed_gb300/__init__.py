@@ -56,6 +56,7 @@ SIGNATURES = {
                                    _P, _ST]),
     "bitdelta_device_status": (_ST, [_P, _P]),
     "bitdelta_check_bounded_wait": (_ST, [_P, ctypes.c_uint32, ctypes.c_int, _P]),
+    "bitdelta_launch_count": (ctypes.c_uint64, []),
     "bitdelta_status_string": (ctypes.c_char_p, [_ST]),
     "bitdelta_abi_version": (ctypes.c_int, []),
 }

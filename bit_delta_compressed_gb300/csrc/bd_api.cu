@@ -1,7 +1,15 @@
 // bd_api.cu -- status handling and small shared host helpers of the C ABI.
+#include <atomic>
+
 #include "bd_internal.cuh"
 
 namespace bd {
+
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+}
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 int sm_count() {
     static int cached[64] = {0};
@@ -47,6 +55,10 @@ extern "C" const char* bitdelta_status_string(bd_status s) {
 }
 
 extern "C" int bitdelta_abi_version(void) { return BITDELTA_ABI_VERSION; }
+
+extern "C" uint64_t bitdelta_launch_count(void) {
+    return bd::g_launches.load(std::memory_order_relaxed);
+}
 
 // ---------------------------------------------------------------------------
 // Health check of the bounded waits the tensor-core kernels use: one thread

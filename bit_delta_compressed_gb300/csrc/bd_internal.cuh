@@ -41,8 +41,14 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
-// Launch check: returns BD_ERR_CUDA if the last launch failed.
+// Kernels this library has enqueued since it was loaded (all devices and
+// streams); bitdelta_launch_count() reads it.
+void note_launch();
+
+// Launch check, called once right after every kernel launch: counts the
+// launch and returns BD_ERR_CUDA if it failed.
 inline bd_status launch_status() {
+    note_launch();
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
 }

@@ -121,14 +121,16 @@ bd_status bitdelta_compress_rows(const void *w_ft, const void *w_base, bd_dtype 
  * workspace; the scratch (one fp64 partial per block, at most 2048 blocks,
  * 16.6 KB) is a static device array inside the library that every GPU
  * loading the library keeps until the process exits.
- *   - The first call on a device looks up that array's device address (with
- *     the device current) and caches it; make that first call before any
- *     stream capture.
+ *   - Every call looks up that array's device address with the current
+ *     device (no allocation).  The first call on a device, and the first
+ *     after a reset of its context, loads the library's device code; make
+ *     that call before any stream capture.
  *   - All calls share the array and it keeps the last call's contents; the
  *     finishing ticket is cleared on the stream before every launch.  Calls
  *     that overlap on the GPU race on the array: order them on one stream.
- *   - A matrix whose launch would need more than 2048 blocks is rejected with
- *     BD_ERR_WORKSPACE before anything is enqueued.
+ *   - The launch uses at most 2048 blocks (one partial each); larger
+ *     matrices are covered by the kernel's grid-stride loop, so any size that
+ *     bitdelta_compress takes is accepted.
  * Calls no allocating routine. */
 bd_status bitdelta_compress_noalloc(const void *w_ft, const void *w_base, bd_dtype in_dtype,
                                     int64_t N, int64_t K, float *alpha_out,
@@ -255,6 +257,11 @@ bd_status bitdelta_device_status(void *workspace, void *stream);
  * bitdelta_device_status.  The device stays usable. */
 bd_status bitdelta_check_bounded_wait(void *workspace, uint32_t poll_limit, int arrive,
                                       void *stream);
+
+/* Kernels this library has enqueued since it was loaded, over all devices
+ * and streams (launches that failed included).  Measurement plumbing; the
+ * page has no counterpart.  Thread-safe; reading it costs no GPU work. */
+uint64_t bitdelta_launch_count(void);
 
 /* Static English text for a status code. */
 const char *bitdelta_status_string(bd_status s);
