@@ -831,12 +831,13 @@ def row_reconstruct(args, torch, bd, wl, dev, pk, g):
 
 def row_delta_cache(args, torch, dev):
     """Delta-cache loads: three variants of 1 GiB of packed bits each (pinned
-    host memory) through a 2 GiB device cache, so every other acquire loads
-    one variant and evicts another; bytes moved host -> device per second on
-    the cache's copy stream."""
+    host memory) through a 2 GiB device cache without a hot set (every
+    variant evictable), so every other acquire loads one variant and evicts
+    another; bytes moved host -> device per second on the cache's copy
+    stream."""
     from bit_delta_compressed_gb300.cache import DeltaCache
     nbits = 1 << 30
-    cache = DeltaCache(2 * nbits + (1 << 20), dev)
+    cache = DeltaCache(2 * nbits + (1 << 20), dev, pinned_top_k=0)
     for i in range(3):
         bits = torch.empty(nbits // 4, dtype=torch.int32).pin_memory()
         bits.fill_(i)
@@ -855,8 +856,41 @@ def row_delta_cache(args, torch, dev):
     torch.cuda.synchronize()
     moved = cache.bytes_loaded - before
     ms = t0.elapsed_time(t1)
-    return {"workload": "3 variants x 1 GiB of bits through a 2 GiB device cache (LRU x rate)",
+    hot = delta_cache_hot_set(torch, dev)
+    return {"hot_set": hot,
+            "workload": "3 variants x 1 GiB of bits through a 2 GiB device cache (LRU x rate, no hot set)",
             "loads": len(order) - 2, "bytes": moved, "ms": ms, "gbs": moved / (ms / 1e3) / 1e9}
+
+
+def delta_cache_hot_set(torch, dev):
+    """The page's residency policy on a request stream: 14 variants of 32 MiB
+    of bits, a device cache with room for 8, 400 acquires whose variants
+    follow a Zipf(1.1) mix (a fake clock advancing 10 ms per request).  Loads
+    and hit rate with the six most requested variants kept resident, beside
+    the same stream through plain rate-weighted LRU."""
+    from bit_delta_compressed_gb300.cache import DeltaCache
+    import workloads as wl
+    V, nbits, reqs = 14, 32 << 20, 400
+    order = wl.variant_ids_zipf(reqs, V, 1.1, wl.generator(77)).tolist()
+    host = [torch.full((nbits // 4,), v, dtype=torch.int32).pin_memory() for v in range(V)]
+    scales = [torch.full((64,), 1e-3).pin_memory() for _ in range(V)]
+    out = {}
+    for k in (6, 0):
+        t = [0.0]
+        cache = DeltaCache(8 * (nbits + 256) + 4096, dev, pinned_top_k=k, clock=lambda: t[0])
+        for v in range(V):
+            cache.register("v%d" % v, [scales[v]], [host[v]])
+        for v in order:
+            t[0] += 0.01
+            cache.release(cache.acquire("v%d" % v))
+        torch.cuda.synchronize()
+        loads = sum(st.loads for st in cache.stats.values())
+        out["top%d" % k] = {"loads": loads, "hit_rate": 1.0 - loads / reqs,
+                            "resident": cache.resident_names()}
+        del cache
+    torch.cuda.empty_cache()
+    out["workload"] = "14 variants x 32 MiB, room for 8, 400 Zipf(1.1) requests"
+    return out
 
 
 def pick_path(bd, preferred, call):

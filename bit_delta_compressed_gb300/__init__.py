@@ -31,10 +31,11 @@ LIB_PATH = _PKG / "libbitdelta.so"
 BD_OK, BD_ERR_NULL, BD_ERR_ALIGN, BD_ERR_SHAPE, BD_ERR_DTYPE, BD_ERR_VARIANT, \
     BD_ERR_WORKSPACE, BD_ERR_CUDA, BD_ERR_TIMEOUT, BD_ERR_UNSUPPORTED = range(10)
 BD_F32, BD_BF16 = 0, 1
-BD_PATH_AUTO, BD_PATH_SIMT, BD_PATH_DECODE_TC, BD_PATH_PREFILL_TC, BD_PATH_DECODE_FOLD = range(5)
+BD_PATH_AUTO, BD_PATH_SIMT, BD_PATH_DECODE_TC, BD_PATH_PREFILL_TC, BD_PATH_DECODE_FOLD, BD_PATH_DECODE_WEFF = range(6)
 MAX_VARIANTS = 64
 PATHS = {"auto": BD_PATH_AUTO, "simt": BD_PATH_SIMT, "decode_tc": BD_PATH_DECODE_TC,
-         "prefill_tc": BD_PATH_PREFILL_TC, "decode_fold": BD_PATH_DECODE_FOLD}
+         "prefill_tc": BD_PATH_PREFILL_TC, "decode_fold": BD_PATH_DECODE_FOLD,
+         "decode_weff": BD_PATH_DECODE_WEFF}
 
 # name -> (restype, argtypes), in the order of include/bitdelta.h
 _P, _I64, _I32, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t

@@ -601,8 +601,9 @@ bd_status prepare(const void* x, int64_t M, int64_t N, int64_t K, const void* w_
     a.y_dtype = y_dtype;
     if (path == BD_PATH_AUTO) path = choose_path(a);
     if (path != BD_PATH_SIMT && path != BD_PATH_DECODE_TC && path != BD_PATH_PREFILL_TC &&
-        path != BD_PATH_DECODE_FOLD)
+        path != BD_PATH_DECODE_FOLD && path != BD_PATH_DECODE_WEFF)
         return BD_ERR_UNSUPPORTED;
+    if (path == BD_PATH_DECODE_WEFF && !decode_weff_supported(a)) return BD_ERR_UNSUPPORTED;
     if (path == BD_PATH_DECODE_TC && !decode_tc_supported(a)) return BD_ERR_UNSUPPORTED;
     if (path == BD_PATH_DECODE_FOLD && !decode_fold_supported(a)) return BD_ERR_UNSUPPORTED;
     if (path == BD_PATH_PREFILL_TC && !prefill_tc_supported(a)) return BD_ERR_UNSUPPORTED;
@@ -617,6 +618,13 @@ bd_path choose_path(const LinearArgs& a) {
     // kernel is faster (4096 x 4096: 11.9 / 14.5 / 24.6 / 26.6 us for 1-4
     // tokens on CUDA cores against 22.5 us on tensor cores)
     if (a.M <= 2) return BD_PATH_SIMT;
+    // One variant (V == 1): bf16 W_eff tiles built in shared memory and the
+    // activations used as they are -- no staging kernel; faster than the
+    // per-variant kernel on every shape measured (4096 x 4096 at 8 to 128
+    // tokens: 19.6 to 23.8 us against 20.9 to 26.7 us, graph-replayed; the
+    // 1024 x 8192, 8192 x 8192 and 28672 x 8192 shapes at 64 tokens by 7 to
+    // 27%)
+    if (a.V == 1 && decode_weff_supported(a)) return BD_PATH_DECODE_WEFF;
     // Measured on GB300 (q, k/v, gate and 4096 x 4096 shapes, 2 to 14 Zipf
     // variants, 16 to 128 tokens): the per-variant sign kernel wins for few
     // variants or few tokens; the folded kernel, whose cost hardly grows with
@@ -640,6 +648,7 @@ bd_status launch_path(bd_path path, const LinearArgs& a, const LinearWorkspace& 
         case BD_PATH_DECODE_TC: return launch_decode_tc(a, w, s);
         case BD_PATH_DECODE_FOLD: return launch_decode_fold(a, w, s);
         case BD_PATH_PREFILL_TC: return launch_prefill_tc(a, w, s);
+        case BD_PATH_DECODE_WEFF: return launch_decode_weff(a, w, s);
         default: return launch_simt(a, w, s);
     }
 }

@@ -32,6 +32,8 @@ bd_path choose_path(const LinearArgs& a);
 bool decode_tc_supported(const LinearArgs& a);
 bool prefill_tc_supported(const LinearArgs& a);
 bool decode_fold_supported(const LinearArgs& a);
+bool decode_weff_supported(const LinearArgs& a);
+bd_status launch_decode_weff(const LinearArgs& a, const LinearWorkspace& w, cudaStream_t s);
 size_t decode_fold_scratch_bytes(int64_t M, int64_t N, int64_t K, int32_t V);
 bd_status launch_decode_fold(const LinearArgs& a, const LinearWorkspace& w, cudaStream_t s);
 bd_status launch_decode_tc(const LinearArgs& a, const LinearWorkspace& w, cudaStream_t s);

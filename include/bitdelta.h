@@ -74,9 +74,12 @@ typedef enum {
                                M <= 176 tokens.  With 2 to 8 K slices and M <= 128 the slices
                                of a 128-row tile launch as one thread-block cluster */
     BD_PATH_PREFILL_TC = 3, /* tcgen05 prefill kernel: W_eff tiles built in shared memory */
-    BD_PATH_DECODE_FOLD = 4 /* tcgen05 decode kernel with one sign accumulator shared by all
+    BD_PATH_DECODE_FOLD = 4, /* tcgen05 decode kernel with one sign accumulator shared by all
                                variants (a column per token), the scales applied in the epilogue:
                                M <= 128 tokens and at most 16 distinct variants */
+    BD_PATH_DECODE_WEFF = 5 /* tcgen05 decode kernel for a single variant (V == 1): bf16 W_eff
+                               tiles built in shared memory, the activations used as they are;
+                               M <= 128 tokens, K % 64 == 0 */
 } bd_path;
 
 /* ------------------------------------------------------------------ */

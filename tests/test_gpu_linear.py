@@ -14,7 +14,7 @@ from tests.gpu_util import assert_y_close, bf16_np, bits_np, f32_np, load_bd
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-PATHS = ["simt", "decode_tc", "prefill_tc", "decode_fold"]
+PATHS = ["simt", "decode_tc", "prefill_tc", "decode_fold", "decode_weff"]
 
 
 @pytest.fixture(scope="module")
@@ -212,3 +212,28 @@ def test_empty_batch(bd):
     wb = torch.zeros((8, 64), dtype=torch.bfloat16, device=DEV)
     y = bd.linear(x, ids, wb, torch.zeros(1, device=DEV), [torch.zeros((8, 2), dtype=torch.int32, device=DEV)])
     assert y.shape == (0, 8)
+
+
+@pytest.mark.parametrize("M", [1, 3, 16, 77, 128])
+def test_single_variant_with_base_and_invalid_tokens(bd, o, M):
+    """One variant (V = 1) with base-model tokens and out-of-range ids mixed
+    in, on the single-variant kernel (which multiplies the base tile for
+    base-model tokens beside the W_eff tile) and the automatic path."""
+    g = wl.generator(900 + M, DEV)
+    N, K = 384, 1024
+    wb = wl.base_weights(N, K, g, DEV)
+    bits = random_bits(g, N, K, 1)
+    alphas = torch.tensor([1.3e-3], device=DEV)
+    x = wl.activations(M, K, g, DEV)
+    ids_h = np.zeros(M, dtype=np.int32)
+    ids_h[1::3] = -1
+    if M > 4:
+        ids_h[4::11] = 7
+    ids = torch.from_numpy(ids_h).to(DEV)
+    bad = (ids_h < -1) | (ids_h >= 1)
+    for path in ("decode_weff", "auto"):
+        y = run(bd, path, x, ids, wb, alphas, bits, expect_status=bd.BD_ERR_VARIANT if bad.any() else 0)
+        assert np.all(y[bad] == 0.0)
+        good = np.nonzero(~bad)[0]
+        ref = o.linear(bf16_np(x)[good], ids_h[good], bf16_np(wb), f32_np(alphas), [bits_np(b) for b in bits])
+        assert_y_close(y[good], ref, "%s M=%d" % (path, M))

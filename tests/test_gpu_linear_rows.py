@@ -16,7 +16,7 @@ from tests.gpu_util import assert_y_close, bf16_np, bits_np, f32_np, load_bd
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-ROW_PATHS = ["auto", "simt", "decode_tc", "prefill_tc", "decode_fold"]
+ROW_PATHS = ["auto", "simt", "decode_tc", "prefill_tc", "decode_fold", "decode_weff"]
 
 
 @pytest.fixture(scope="module")
@@ -143,3 +143,19 @@ def test_prefill_materialised(bd, o, per_row):
         ref = o.linear(bf16_np(x), ids.cpu().numpy(), bf16_np(wb), f32_np(al), [bits_np(b) for b in bits],
                        rows=rows)
     assert_y_close(y.astype(np.float64)[:, rows], ref, "prefill materialised per_row=%s" % per_row)
+
+
+@pytest.mark.parametrize("M", [1, 8, 64])
+def test_rows_single_variant(bd, o, M):
+    """Per-row scales on the single-variant kernel (V = 1), base-model tokens
+    mixed in, a 2048 x 4096 matrix split over several K slices."""
+    g = wl.generator(140 + M, DEV)
+    N, K = 2048, 4096
+    wb, arows, bits = row_case(bd, g, N, K, 1)
+    x = wl.activations(M, K, g, DEV)
+    ids = torch.zeros(M, dtype=torch.int32, device=DEV)
+    ids[::5] = -1
+    y = run_rows(bd, "decode_weff", x, ids, wb, arows, bits)
+    rows = np.arange(0, N, 7)
+    ref = oracle_rows(o, x, ids, wb, arows, bits, rows)
+    assert_y_close(y[:, rows], ref, "rows single variant M=%d" % M)

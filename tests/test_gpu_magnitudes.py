@@ -138,3 +138,17 @@ def test_mixed_magnitudes_many_variants(bd, o, path):
     ids = wl.variant_ids_zipf(M, V, 1.1, wl.generator(721))
     ids[::11] = -1
     run_case(bd, o, path, x, ids.to(DEV), wb, alphas, bits)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_one_kind_single_variant(bd, o, kind):
+    """The single-variant kernel (bf16 W_eff tiles, the activations used as
+    they are) on every token kind, with base-model tokens."""
+    g = wl.generator(760 + KINDS.index(kind), DEV)
+    M, N, K = 16, 256, 4096
+    wb = wl.base_weights(N, K, g, DEV)
+    bits = random_bits(g, N, K, 1)
+    alphas = torch.tensor([1.5e-3], device=DEV)
+    x = build_batch([kind] * M, K, g)
+    ids = torch.tensor([0, 0, -1, 0] * 4, dtype=torch.int32, device=DEV)
+    run_case(bd, o, "decode_weff", x, ids, wb, alphas, bits)
