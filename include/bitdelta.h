@@ -9,7 +9,10 @@
  *   section "Serving architecture": many fine-tuned variants share one
  *     resident base; a fused kernel reads the base weights and the packed
  *     delta bits together and never writes W_eff to HBM (the conceptual
- *     fused_bitdelta_linear listing: reconstruct, then linear);
+ *     fused_bitdelta_linear listing: reconstruct, then linear).  The decode
+ *     paths here never write W_eff; the prefill path writes it, once per
+ *     present variant and into the caller's workspace, when the batch has at
+ *     least 2048 tokens per present variant (see BD_PATH_PREFILL_TC);
  *   section "Infrastructure details": sign bits packed 8 per byte (a
  *     4096 x 4096 weight packs to 4096 x 512 bytes), alpha stored as f32.
  *
@@ -73,7 +76,11 @@ typedef enum {
     BD_PATH_DECODE_TC = 2,  /* tcgen05 decode kernel: base and sign products on tensor cores;
                                M <= 176 tokens.  With 2 to 8 K slices and M <= 128 the slices
                                of a 128-row tile launch as one thread-block cluster */
-    BD_PATH_PREFILL_TC = 3, /* tcgen05 prefill kernel: W_eff tiles built in shared memory */
+    BD_PATH_PREFILL_TC = 3, /* tcgen05 prefill kernel.  With at least 2048 tokens per present
+                               variant (M / min(V, M) >= 2048, and at most 32 GiB of W_eff) every
+                               present variant's W_eff (nearest bf16) is first written to the
+                               workspace, one HBM pass per variant, and the GEMM loads it; with
+                               fewer tokens bf16 W_eff tiles are built in shared memory */
     BD_PATH_DECODE_FOLD = 4, /* tcgen05 decode kernel with one sign accumulator shared by all
                                variants (a column per token), the scales applied in the epilogue:
                                M <= 128 tokens and at most 16 distinct variants */
@@ -161,10 +168,16 @@ bd_status bitdelta_reconstruct(const void *w_base, const float *alpha, int32_t p
 /* ------------------------------------------------------------------ */
 /* Multi-variant fused linear ("Serving architecture": W_eff =         */
 /* W_base + alpha_v * sign(delta_v), reconstructed on the fly and fused */
-/* with the matmul, never written to HBM).                              */
+/* with the matmul; the decode paths never write it to HBM, the prefill */
+/* path may, see BD_PATH_PREFILL_TC).                                   */
 /* ------------------------------------------------------------------ */
 
-/* Bytes of device workspace bitdelta_linear needs for this shape. */
+/* Bytes of device workspace bitdelta_linear needs for this shape.  Besides
+ * the grouping and the staged activations of the tensor-core paths this
+ * includes, when the prefill path would materialise W_eff (M / min(V, M) >=
+ * 2048 tokens per present variant), min(V, M) * N * K * 2 bytes for the
+ * materialised bf16 weights -- 1.9 GB for four variants of a 28672 x 8192
+ * matrix. */
 size_t bitdelta_linear_workspace(int64_t M, int64_t N, int64_t K, int32_t V);
 
 /* y[t, n] = sum_k x[t,k] * (W_base[n,k] + alpha_{v(t)} * s_{v(t)}[n,k]),
