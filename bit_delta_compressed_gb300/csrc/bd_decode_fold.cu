@@ -25,11 +25,12 @@
 // One CTA owns 128 output rows (the 128 lanes of tensor memory) and a slice
 // of K (split-K at even 64-column blocks, summed in a fixed order by the CTA
 // that finishes the tile last).  Warps:
-//   * 0, 1, 2 (TMA producers, each with a ring of its own): W_base tiles
-//     (128 x 64 bf16, 128-byte swizzle) from HBM; per 64-column block the
-//     scaled activations X_c (pad16(M) rows) and the sign operand X_p (R rows)
-//     from L2; per pair of blocks one 128-row x 4-word tile of packed bits per
-//     present variant from HBM;
+//   * 0, 1, 2 (producers, each with a ring of its own): W_base tiles
+//     (128 x 64 bf16, 128-byte swizzle) from HBM by TMA; per 64-column block
+//     the scaled activations X_c (pad16(M) rows) and the sign operand X_p (R
+//     rows) from L2 in one bulk copy of a pre-swizzled stage image; per pair
+//     of blocks one 128-row x 4-word tile of packed bits per present variant
+//     from HBM by TMA;
 //   * 3, the base issuer: per block four bf16 MMAs (N = pad16(M)) of the W
 //     tile with X_c; the only consumer of the W ring;
 //   * four issuer groups of five warps.  Group g owns the sign-accumulator
@@ -81,9 +82,6 @@ static_assert(kAEntries >= kFoldSepEntries, "tensor memory budget");
 
 struct FoldParams {
     CUtensorMap tm_w;                           // W_base [N, K] bf16, box 128 rows
-    CUtensorMap tm_xc;                          // X_c [Mb, K] bf16, box Mb rows
-    CUtensorMap tm_xp16;                        // X_p [Rmax, 2K] bytes, box 16 rows
-    CUtensorMap tm_xp128;                       // the same, box 128 rows
     CUtensorMap tm_bits[BITDELTA_MAX_VARIANTS];  // packed bits [N, K/32] u32, box 128 rows x 4 words
     const SegPlan* plan;
     const FoldPlan* fold;
@@ -97,6 +95,7 @@ struct FoldParams {
     unsigned* tickets;
     unsigned* status;
     unsigned* diag;
+    const uint8_t* ximg;                        // per 64-column block, the stage image of X_c and X_p
     int M, N, K, Mb, Rmax, splits, y_bf16;
     int wstages, xstages, bslots;               // ring depths; variants per bits stage
 };
@@ -452,24 +451,20 @@ __global__ void __launch_bounds__(kThreads, 1) fold_decode_kernel(const __grid_c
             }
         }
     } else if (warp == 1) {
-        // ---------------- TMA producer: activations (L2) ----------------
+        // ---------------- bulk producer: activations (L2) ----------------
+        // The staging kernel lays out, per 64-column block, the stage exactly
+        // as it sits in shared memory (X_c rows, then X_p rows, 128-byte
+        // swizzled), so one contiguous copy fills a stage: the copy engine's
+        // cost is per copy and per box row far more than per byte.
         if (lane == 0) {
-            prefetch_tensormap(&p.tm_xc);
-            prefetch_tensormap(&p.tm_xp16);
-            prefetch_tensormap(&p.tm_xp128);
-            const int R = fp.R;
+            const uint32_t bytes = static_cast<uint32_t>(Mb + fp.R) * 128u;
             int issued = 0;
             for (int i = 0; i < nkb; ++i) {
                 const int kb = kb0 + i;
                 const int xs = i % p.xstages;
                 if (!mbar_wait_sleep(&x_empty[xs], ((i / p.xstages) & 1) ^ 1, kWaitLimit, p.status, 22, p.diag)) break;
-                uint8_t* sx = xring + xs * xs_bytes;
-                mbar_expect_tx(&x_full[xs], static_cast<uint32_t>(Mb + R) * 128u);
-                tma_load_2d(sx, &p.tm_xc, &x_full[xs], kb * kBK, 0);
-                uint8_t* sxp = sx + Mb * 128;
-                int r = 0;
-                for (; r + 128 <= R; r += 128) tma_load_2d(sxp + r * 128, &p.tm_xp128, &x_full[xs], kb * 128, r);
-                for (; r < R; r += 16) tma_load_2d(sxp + r * 128, &p.tm_xp16, &x_full[xs], kb * 128, r);
+                mbar_expect_tx(&x_full[xs], bytes);
+                bulk_load(xring + xs * xs_bytes, p.ximg + static_cast<int64_t>(kb) * xs_bytes, bytes, &x_full[xs]);
                 issued = i + 1;
             }
             for (int s = 0; s < p.xstages && s < issued; ++s) {
@@ -591,14 +586,17 @@ __global__ void __launch_bounds__(kThreads, 1) fold_decode_kernel(const __grid_c
 }
 
 // ---------------------------------------------------------------------------
-// Staging for one linear (one block per staged row):
-//   X_c [Mb, K] bf16: grouped order, row p = x[t] * 2^s_t (zero rows past the
-//       valid tokens);
-//   X_p [R, 2K] bytes: entry rows of the plan; row j of entry e holds, if
-//       grouped position e_col + j is a token of the entry's variant v,
-//       x[t] 2^s_t as e4m3 hi and lo, per 64-column block 64 bytes of hi then
-//       64 of lo, byte 32w + 4j + b of a half holding column 32w + j + 8b;
-//       otherwise zeros;
+// Staging for one linear (one block per staged row), written as K / 64 stage
+// images of Mb + Rmax rows x 128 bytes, one per 64-column block, each laid
+// out as the kernel's shared-memory stage (row q at 128 q, its 16-byte chunk
+// c at chunk position c ^ (q & 7): the 128-byte swizzle):
+//   X_c rows [0, Mb) bf16: grouped order, row p = x[t] * 2^s_t (zero rows
+//       past the valid tokens);
+//   X_p rows Mb + [0, R) bytes: entry rows of the plan; row j of entry e
+//       holds, if grouped position e_col + j is a token of the entry's
+//       variant v, x[t] 2^s_t as e4m3 hi and lo, per block 64 bytes of hi
+//       then 64 of lo, byte 32w + 4j + b of a half holding column
+//       32w + j + 8b; otherwise zeros;
 //   s_t = 7 - floor(log2(max_k |x[t,k]|)) (0 for zero rows), clamped to
 //       [-120, 120];
 //   the split-K tickets zeroed.
@@ -634,13 +632,23 @@ __device__ __forceinline__ int scale_exponent(float xmax) {
     return max(-120, min(120, 7 - e));
 }
 
+// 16-byte unit `chunk` of staged row q's 2K bytes in the stage images: block
+// kb = chunk / 8 holds the row at bytes (kb img_rows + q) 128, its chunk
+// c = chunk % 8 at chunk position c ^ (q & 7) (the 128-byte swizzle of a
+// 1024-byte aligned stage).
+__device__ __forceinline__ uint4* image_chunk(uint8_t* ximg, int img_rows, int q, int64_t chunk) {
+    const int64_t kb = chunk >> 3;
+    const int c = static_cast<int>(chunk & 7);
+    return reinterpret_cast<uint4*>(ximg + (kb * img_rows + q) * 128 + ((c ^ (q & 7)) << 4));
+}
+
 __global__ void __launch_bounds__(256) fold_prep_kernel(const uint4* __restrict__ x, int K, int M, int Mb,
                                                         const SegPlan* __restrict__ plan,
                                                         const FoldPlan* __restrict__ fold,
                                                         const int32_t* __restrict__ pos2tok,
                                                         const int32_t* __restrict__ pos_var,
-                                                        int32_t* __restrict__ sexp, uint4* __restrict__ xc,
-                                                        uint4* __restrict__ xp, unsigned* tickets, int n_tickets) {
+                                                        int32_t* __restrict__ sexp, uint8_t* __restrict__ ximg,
+                                                        int img_rows, unsigned* tickets, int n_tickets) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int rr = blockIdx.x;
     const int64_t vec_per_row = K / 8;
@@ -650,9 +658,9 @@ __global__ void __launch_bounds__(256) fold_prep_kernel(const uint4* __restrict_
     if (rr < Mb) {
         const int pos = rr;
         const int tok = pos < n_valid ? pos2tok[pos] : -1;
-        uint4* dst = xc + static_cast<int64_t>(pos) * vec_per_row;
         if (tok < 0) {
-            for (int64_t i = threadIdx.x; i < vec_per_row; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
+            for (int64_t i = threadIdx.x; i < vec_per_row; i += blockDim.x)
+                *image_chunk(ximg, img_rows, pos, i) = make_uint4(0, 0, 0, 0);
             if (threadIdx.x == 0) sexp[pos] = 0;
             return;
         }
@@ -670,7 +678,7 @@ __global__ void __launch_bounds__(256) fold_prep_kernel(const uint4* __restrict_
                     w4[k] = *reinterpret_cast<const uint32_t*>(&pr);
                 }
             }
-            dst[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            *image_chunk(ximg, img_rows, pos, i) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
         return;
     }
@@ -686,9 +694,10 @@ __global__ void __launch_bounds__(256) fold_prep_kernel(const uint4* __restrict_
             break;
         }
     }
-    uint4* dst = xp + static_cast<int64_t>(r) * vec_per_row;    // 2K bytes: hi and lo per block
+    const int q = Mb + r;                                        // 2K bytes: hi and lo per block
     if (tok < 0) {
-        for (int64_t i = threadIdx.x; i < vec_per_row; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
+        for (int64_t i = threadIdx.x; i < vec_per_row; i += blockDim.x)
+            *image_chunk(ximg, img_rows, q, i) = make_uint4(0, 0, 0, 0);
         return;
     }
     const uint4* src = x + static_cast<int64_t>(tok) * vec_per_row;
@@ -697,7 +706,6 @@ __global__ void __launch_bounds__(256) fold_prep_kernel(const uint4* __restrict_
     // one thread per 32-column group: 64 source bytes in, 32 bytes of hi and
     // 32 of lo out; output word jj holds columns jj, jj + 8, jj + 16, jj + 24
     // (converted two at a time)
-    uint8_t* dstb = reinterpret_cast<uint8_t*>(dst);
     for (int grp = threadIdx.x; grp < K / 32; grp += blockDim.x) {
         float v[32];
 #pragma unroll
@@ -727,12 +735,12 @@ __global__ void __launch_bounds__(256) fold_prep_kernel(const uint4* __restrict_
             hi[jj] = hw;
             lo[jj] = lw;
         }
-        uint4* oh = reinterpret_cast<uint4*>(dstb + 128 * (grp >> 1) + 32 * (grp & 1));
-        uint4* ol = reinterpret_cast<uint4*>(dstb + 128 * (grp >> 1) + 64 + 32 * (grp & 1));
-        oh[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        oh[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-        ol[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        ol[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+        // block grp / 2: hi at bytes 32 (grp & 1) .. +32, lo at 64 + the same
+        const int64_t c0 = 8 * static_cast<int64_t>(grp >> 1) + 2 * (grp & 1);
+        *image_chunk(ximg, img_rows, q, c0) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *image_chunk(ximg, img_rows, q, c0 + 1) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+        *image_chunk(ximg, img_rows, q, c0 + 4) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        *image_chunk(ximg, img_rows, q, c0 + 5) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
     }
 }
 
@@ -794,8 +802,7 @@ FoldSmem fold_smem(int Mb, int rmax, int dmax) {
 }
 
 struct FoldScratch {
-    uint16_t* xc;
-    uint8_t* xp;
+    uint8_t* ximg;
     int32_t* sexp;
     float* part;
     unsigned* tickets;
@@ -812,8 +819,8 @@ FoldScratch fold_scratch(void* base, int64_t M, int64_t N, int64_t K, int32_t V,
         return r;
     };
     const int Mb = pad16(static_cast<int>(M));
-    d.xc = reinterpret_cast<uint16_t*>(take(static_cast<size_t>(Mb) * K * 2));
-    d.xp = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(fold_rmax(M, V)) * K * 2));
+    // (K / 64) stage images of (Mb + Rmax) rows x 128 bytes
+    d.ximg = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(Mb + fold_rmax(M, V)) * K * 2));
     d.sexp = reinterpret_cast<int32_t*>(take(static_cast<size_t>(Mb) * 4));
     const int64_t n_tiles = (N + kBN - 1) / kBN;
     d.part = splits > 1 ? reinterpret_cast<float*>(take(static_cast<size_t>(splits) * M * N * 4)) : nullptr;
@@ -850,18 +857,14 @@ bd_status launch_decode_fold(const LinearArgs& a, const LinearWorkspace& w, cuda
     const int rmax = fold_rmax(a.M, a.V);
 
     fold_prep_kernel<<<Mb + rmax, 256, 0, s>>>(static_cast<const uint4*>(a.x), K, M, Mb, w.g.plan,
-                                              w.g.fold, w.g.pos2tok, w.g.pos_var, sc.sexp,
-                                              reinterpret_cast<uint4*>(sc.xc), reinterpret_cast<uint4*>(sc.xp),
+                                              w.g.fold, w.g.pos2tok, w.g.pos_var, sc.sexp, sc.ximg, Mb + rmax,
                                               sc.tickets, splits > 1 ? static_cast<int>(n_tiles) : 0);
     if (launch_status() != BD_OK) return BD_ERR_CUDA;
 
     FoldParams p;
     memset(&p, 0, sizeof p);
-    if (!make_tmap_bf16_sw128(&p.tm_w, a.w_base, a.N, a.K, kBN) ||
-        !make_tmap_bf16_sw128(&p.tm_xc, sc.xc, Mb, a.K, Mb) ||
-        !make_tmap_u8_sw128(&p.tm_xp16, sc.xp, rmax, 2 * a.K, 16) ||
-        !make_tmap_u8_sw128(&p.tm_xp128, sc.xp, rmax, 2 * a.K, 128))
-        return BD_ERR_CUDA;
+    if (!make_tmap_bf16_sw128(&p.tm_w, a.w_base, a.N, a.K, kBN)) return BD_ERR_CUDA;
+    p.ximg = sc.ximg;
     for (int v = 0; v < a.V; ++v)
         if (!make_tmap_bits(&p.tm_bits[v], a.bits.p[v], a.N, a.K / 32, kBN)) return BD_ERR_CUDA;
     p.plan = w.g.plan;
