@@ -344,12 +344,51 @@ __global__ void __launch_bounds__(kThreads, 1) weff_decode_kernel(const __grid_c
     }
 }
 
-// K slices per row tile: enough CTAs to cover the SMs once (at most 8, the
-// cluster size), each slice at least 8 blocks.
-int weff_splits(int64_t n_tiles, int kb_total, int sms) {
-    int s = 1;
-    while (s < kMaxSplits && n_tiles * (s + 1) <= sms && kb_total / (s + 1) >= 8) ++s;
-    return s;
+// Clusters of `s` CTAs (one per SM at this kernel's shared-memory size) that
+// run at once: the GPCs' SM counts need not be multiples of s.  Cached per
+// device; 0 if the query fails.
+int cluster_capacity(int s, int smem) {
+    static int cache[64][kMaxSplits + 1] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cache[dev][s] > 0) return cache[dev][s];
+    if (s == 1) return cache[dev][1] = sm_count();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(s * 64));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(s);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, weff_decode_kernel, &cfg) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        return 0;
+    }
+    return cache[dev][s] = n;
+}
+
+// K slices per row tile (at most 8, the cluster size; each slice at least 8
+// blocks): the fewest block-times on the busiest SM, counting whole waves of
+// clusters -- waves x (blocks per slice + about six blocks' worth of fixed
+// cost per CTA).  A 224-tile matrix (28672 rows) thus runs in slices of 64
+// blocks rather than in two waves of 128.
+int weff_splits(int64_t n_tiles, int kb_total, int smem) {
+    constexpr int64_t kFixedBlocks = 6;
+    int best = 1;
+    int64_t best_cost = -1;
+    for (int s = 1; s <= kMaxSplits && (s == 1 || kb_total / s >= 8); ++s) {
+        const int cap = cluster_capacity(s, smem);          // clusters at once
+        if (cap < 1) continue;
+        const int64_t waves = (n_tiles + cap - 1) / cap;
+        const int64_t cost = waves * ((kb_total + s - 1) / s + kFixedBlocks);
+        if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = s; }
+    }
+    return best;
 }
 
 }  // namespace
@@ -363,7 +402,9 @@ bd_status launch_decode_weff(const LinearArgs& a, const LinearWorkspace& w, cuda
     const int M = static_cast<int>(a.M);
     const int Mb = pad16(M);
     const int64_t n_tiles = (a.N + kBN - 1) / kBN;
-    const int splits = weff_splits(n_tiles, static_cast<int>(a.K / kBK), sm_count());
+    const int smem = static_cast<int>(smem_bytes(Mb));
+    if (!set_smem_attr(reinterpret_cast<const void*>(weff_decode_kernel), smem, 3)) return BD_ERR_CUDA;
+    const int splits = weff_splits(n_tiles, static_cast<int>(a.K / kBK), smem);
     WeffParams p;
     memset(&p, 0, sizeof p);
     if (!make_tmap_bf16_sw128(&p.tm_w, a.w_base, a.N, a.K, kBN) ||
@@ -384,8 +425,6 @@ bd_status launch_decode_weff(const LinearArgs& a, const LinearWorkspace& w, cuda
     p.Mb = Mb;
     p.splits = splits;
     p.y_bf16 = (a.y_dtype == BD_BF16);
-    const int smem = static_cast<int>(smem_bytes(Mb));
-    if (!set_smem_attr(reinterpret_cast<const void*>(weff_decode_kernel), smem, 3)) return BD_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(n_tiles * splits));
     cfg.blockDim = dim3(kThreads);
