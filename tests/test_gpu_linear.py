@@ -237,3 +237,23 @@ def test_single_variant_with_base_and_invalid_tokens(bd, o, M):
         good = np.nonzero(~bad)[0]
         ref = o.linear(bf16_np(x)[good], ids_h[good], bf16_np(wb), f32_np(alphas), [bits_np(b) for b in bits])
         assert_y_close(y[good], ref, "%s M=%d" % (path, M))
+
+
+@pytest.mark.parametrize("M", [8, 64])
+@pytest.mark.parametrize("N,K", [(28672, 8192), (8192, 28672), (8192, 8192)])
+def test_single_variant_full_shapes(bd, o, N, K, M):
+    """The single-variant kernel on the 70B stack's shapes, where its K split
+    comes from the clusters that fit at once (two or more slices per row
+    tile), with base-model tokens mixed in; 64 sampled output rows, all
+    tokens."""
+    g = wl.generator(950 + M + N // 1024, DEV)
+    wb = wl.base_weights(N, K, g, DEV)
+    bits = random_bits(g, N, K, 1)
+    alphas = torch.tensor([8e-4], device=DEV)
+    x = wl.activations(M, K, g, DEV)
+    ids = torch.zeros(M, dtype=torch.int32, device=DEV)
+    ids[::7] = -1
+    y = run(bd, "decode_weff", x, ids, wb, alphas, bits, out_dtype=torch.bfloat16)
+    rows = np.sort(np.random.default_rng(951).choice(N, 64, replace=False))
+    ref = oracle_y(o, x, ids, wb, alphas, bits, rows)
+    assert_y_close(y[:, rows], ref, "single variant %dx%d M=%d" % (N, K, M))
