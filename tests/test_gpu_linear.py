@@ -257,3 +257,38 @@ def test_single_variant_full_shapes(bd, o, N, K, M):
     rows = np.sort(np.random.default_rng(951).choice(N, 64, replace=False))
     ref = oracle_y(o, x, ids, wb, alphas, bits, rows)
     assert_y_close(y[:, rows], ref, "single variant %dx%d M=%d" % (N, K, M))
+
+
+@pytest.mark.parametrize("M,N,K,V", [(1, 1000, 128, 1), (2, 777, 4096, 1), (3, 4096, 4096, 3), (5, 300, 1024, 2),
+                                     (8, 2048, 4096, 1), (8, 1500, 4096, 5), (4, 1024, 8192, 2), (1, 512, 28672, 1)])
+@pytest.mark.parametrize("per_row", [False, True])
+def test_small_batch_cuda_cores(bd, o, M, N, K, V, per_row):
+    """1 to 8 tokens on the CUDA-core path: ragged row counts, K from 128 to
+    28672, one or several variants, base-model tokens and out-of-range ids
+    mixed in, per-matrix and per-row scales."""
+    g = wl.generator(970 + M * 7 + V + int(per_row), DEV)
+    wb = wl.base_weights(N, K, g, DEV)
+    bits = random_bits(g, N, K, V)
+    x = wl.activations(M, K, g, DEV)
+    ids_h = np.arange(M, dtype=np.int32) % V
+    if M >= 3:
+        ids_h[1] = -1
+    if M >= 5:
+        ids_h[3] = V + 2
+    ids = torch.from_numpy(ids_h).to(DEV)
+    bad = (ids_h < -1) | (ids_h >= V)
+    if per_row:
+        alphas = (2e-4 + 1.8e-3 * torch.rand(V, N, generator=g, device=DEV)).contiguous()
+        ws = bd.linear_workspace(M, N, K, V, DEV)
+        y = bd.linear_rows(x, ids, wb, alphas, bits, workspace=ws, path="simt")
+        assert bd.device_status(ws) == (bd.BD_ERR_VARIANT if bad.any() else 0)
+        y = y.float().cpu().numpy().astype(np.float64)
+    else:
+        alphas = 2e-4 + 1.8e-3 * torch.rand(V, generator=g, device=DEV)
+        y = run(bd, "simt", x, ids, wb, alphas, bits, expect_status=bd.BD_ERR_VARIANT if bad.any() else 0)
+    assert np.all(y[bad] == 0.0)
+    good = np.nonzero(~bad)[0]
+    rows = np.arange(N) if N <= 1024 else np.sort(np.random.default_rng(971).choice(N, 256, replace=False))
+    ref = o.linear(bf16_np(x)[good], ids_h[good], bf16_np(wb), f32_np(alphas), [bits_np(b) for b in bits],
+                   rows=rows, per_row_alpha=per_row)
+    assert_y_close(y[good][:, rows], ref, "cuda cores M=%d N=%d K=%d V=%d rows=%s" % (M, N, K, V, per_row))
