@@ -414,20 +414,28 @@ simt_linear_kernel(const uint4* __restrict__ x, const uint4* __restrict__ w_base
 }
 
 // ---------------------------------------------------------------------------
-// Small-batch CUDA-core path (M <= 4): a GEMV per output row.  One warp per
-// row; each lane issues U 16-byte weight loads (plus the matching activation
-// vectors and bits bytes) before doing any arithmetic, so enough bytes are in
-// flight per SM to stream W_base at full HBM bandwidth.
+// Small-batch CUDA-core path (M <= 4): a GEMV per output row.  `split` warps
+// (1, 2, 4 or 8) share a row, each taking a contiguous 1/split of its
+// 8-column chunks; each lane issues U 16-byte weight loads (plus the matching
+// activation vectors and bits bytes) before doing any arithmetic, so enough
+// bytes are in flight per SM to stream W_base at full HBM bandwidth.  Narrow
+// matrices use split > 1 so that every SM holds enough warps and each warp
+// makes fewer dependent round trips; the parts of a row are added in a fixed
+// order.
 // ---------------------------------------------------------------------------
-template <int MT, int U>
+template <int MT, int U, int SPLIT>
 __global__ void __launch_bounds__(kSimtWarps * 32)
 gemv_kernel(const uint4* __restrict__ x, const uint4* __restrict__ w_base,
             const float* __restrict__ alphas, int alpha_rows, BitsTable bt, int M, int64_t N, int64_t K,
             GroupView g, void* y, int y_bf16) {
-    const int lane = threadIdx.x & 31;
-    const int64_t n = static_cast<int64_t>(blockIdx.x) * kSimtWarps + (threadIdx.x >> 5);
-    if (n >= N) return;
+    __shared__ float part_sum[SPLIT > 1 ? kSimtWarps : 1][2 * MT];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int part = warp % SPLIT;
+    const int64_t n = static_cast<int64_t>(blockIdx.x) * (kSimtWarps / SPLIT) + warp / SPLIT;
+    const bool row_ok = n < N;
+    if (SPLIT == 1 && !row_ok) return;                      // no block-wide barrier below
     const int64_t kc = K / 8;
+    const int64_t c_lo = SPLIT == 1 ? 0 : kc * part / SPLIT, c_hi = SPLIT == 1 ? kc : kc * (part + 1) / SPLIT;
     int tok[MT], var[MT];
     const uint8_t* bp[MT];
 #pragma unroll
@@ -435,12 +443,12 @@ gemv_kernel(const uint4* __restrict__ x, const uint4* __restrict__ w_base,
         tok[j] = (j < M) ? g.pos2tok[j] : -1;
         var[j] = (j < M) ? g.pos_var[j] : -2;
         if (var[j] == -2) tok[j] = -1;                      // invalid id: zero row
-        bp[j] = (var[j] >= 0) ? bt.p[var[j]] + n * kc : nullptr;
+        bp[j] = (var[j] >= 0 && (SPLIT == 1 || row_ok)) ? bt.p[var[j]] + n * kc : nullptr;
     }
     float accb[MT], accs[MT];
 #pragma unroll
     for (int j = 0; j < MT; ++j) { accb[j] = 0.f; accs[j] = 0.f; }
-    const uint4* wrow = w_base + n * kc;
+    const uint4* wrow = w_base + (SPLIT == 1 || row_ok ? n : 0) * kc;
     auto chunk = [&](const uint4& wv, const uint4 (&xv)[MT], const uint32_t (&bb)[MT]) {
         const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
         float wf[8];
@@ -463,8 +471,9 @@ gemv_kernel(const uint4* __restrict__ x, const uint4* __restrict__ w_base,
             accs[j] += ds;
         }
     };
-    int64_t c = lane;
-    for (; c + 32 * (U - 1) < kc; c += 32 * U) {
+    int64_t c = c_lo + lane;
+    const int64_t c_end = (SPLIT == 1 || row_ok) ? c_hi : c_lo;   // a row past N does no work
+    for (; c + 32 * (U - 1) < c_end; c += 32 * U) {
         uint4 wv[U];
         uint4 xv[U][MT];
         uint32_t bb[U][MT];
@@ -480,7 +489,7 @@ gemv_kernel(const uint4* __restrict__ x, const uint4* __restrict__ w_base,
 #pragma unroll
         for (int u = 0; u < U; ++u) chunk(wv[u], xv[u], bb[u]);
     }
-    for (; c < kc; c += 32) {
+    for (; c < c_end; c += 32) {
         uint4 xv[MT];
         uint32_t bb[MT];
         const uint4 wv = ld_stream(wrow + c);
@@ -498,6 +507,24 @@ gemv_kernel(const uint4* __restrict__ x, const uint4* __restrict__ w_base,
             accb[j] += __shfl_xor_sync(0xffffffffu, accb[j], o);
             accs[j] += __shfl_xor_sync(0xffffffffu, accs[j], o);
         }
+    }
+    if (SPLIT > 1) {
+        // the parts of a row, added in order 0, 1, ... by the row's first warp
+        if (lane == 0)
+#pragma unroll
+            for (int j = 0; j < MT; ++j) {
+                part_sum[warp][j] = accb[j];
+                part_sum[warp][MT + j] = accs[j];
+            }
+        __syncthreads();
+        if (part != 0 || !row_ok) return;
+        if (lane == 0)
+            for (int q = 1; q < SPLIT; ++q)
+#pragma unroll
+                for (int j = 0; j < MT; ++j) {
+                    accb[j] += part_sum[warp + q][j];
+                    accs[j] += part_sum[warp + q][MT + j];
+                }
     }
     if (lane == 0) {
 #pragma unroll
@@ -525,6 +552,35 @@ bd_status launch_group(const int32_t* ids, int64_t M, int32_t V, const LinearWor
     return launch_status();
 }
 
+// Warps of gemv_kernel<MT, U> that run at once on the device (cached per
+// device and instantiation).
+template <int MT, int U>
+int64_t gemv_resident_warps() {
+    // every SPLIT uses the same registers within a few; the unsplit kernel decides
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cache[dev] == 0) {
+        int nb = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, gemv_kernel<MT, U, 2>, kSimtWarps * 32, 0) != cudaSuccess ||
+            nb < 1) {
+            cudaGetLastError();
+            nb = 1;
+        }
+        cache[dev] = nb;
+    }
+    return static_cast<int64_t>(cache[dev]) * kSimtWarps * sm_count();
+}
+
+// Warps per GEMV row: the most (1 to 8) that keep every warp of the launch
+// resident at once and give each at least one full round of U 16-byte loads
+// per lane.
+int gemv_split(int64_t N, int64_t K, int U, int64_t resident) {
+    int split = 1;
+    while (split < kSimtWarps && N * split * 2 <= resident && (K / 8) / (split * 2) >= 32 * U) split *= 2;
+    return split;
+}
+
 bd_status launch_simt(const LinearArgs& a, const LinearWorkspace& w, cudaStream_t s) {
     const int64_t blocks = (a.N + kSimtWarps - 1) / kSimtWarps;
     if (a.M <= 4) {
@@ -532,10 +588,32 @@ bd_status launch_simt(const LinearArgs& a, const LinearWorkspace& w, cudaStream_
         const uint4* wb = static_cast<const uint4*>(a.w_base);
         const int M = static_cast<int>(a.M);
         const int yb = a.y_dtype == BD_BF16;
-        const unsigned grid = static_cast<unsigned>(blocks);
-        if (a.M == 1) gemv_kernel<1, 4><<<grid, kSimtWarps * 32, 0, s>>>(xx, wb, a.alphas, a.alpha_rows, a.bits, M, a.N, a.K, w.g, a.y, yb);
-        else if (a.M == 2) gemv_kernel<2, 4><<<grid, kSimtWarps * 32, 0, s>>>(xx, wb, a.alphas, a.alpha_rows, a.bits, M, a.N, a.K, w.g, a.y, yb);
-        else gemv_kernel<4, 2><<<grid, kSimtWarps * 32, 0, s>>>(xx, wb, a.alphas, a.alpha_rows, a.bits, M, a.N, a.K, w.g, a.y, yb);
+        const int U = a.M <= 2 ? 4 : 2;
+        const int64_t resident = a.M == 1   ? gemv_resident_warps<1, 4>()
+                                 : a.M == 2 ? gemv_resident_warps<2, 4>()
+                                            : gemv_resident_warps<4, 2>();
+        const int split = gemv_split(a.N, a.K, U, resident);
+        const int rows_per_block = kSimtWarps / split;
+        const unsigned grid = static_cast<unsigned>((a.N + rows_per_block - 1) / rows_per_block);
+        auto go = [&](auto kern) {
+            kern<<<grid, kSimtWarps * 32, 0, s>>>(xx, wb, a.alphas, a.alpha_rows, a.bits, M, a.N, a.K, w.g, a.y, yb);
+        };
+        if (a.M == 1) {
+            if (split == 1) go(gemv_kernel<1, 4, 1>);
+            else if (split == 2) go(gemv_kernel<1, 4, 2>);
+            else if (split == 4) go(gemv_kernel<1, 4, 4>);
+            else go(gemv_kernel<1, 4, 8>);
+        } else if (a.M == 2) {
+            if (split == 1) go(gemv_kernel<2, 4, 1>);
+            else if (split == 2) go(gemv_kernel<2, 4, 2>);
+            else if (split == 4) go(gemv_kernel<2, 4, 4>);
+            else go(gemv_kernel<2, 4, 8>);
+        } else {
+            if (split == 1) go(gemv_kernel<4, 2, 1>);
+            else if (split == 2) go(gemv_kernel<4, 2, 2>);
+            else if (split == 4) go(gemv_kernel<4, 2, 4>);
+            else go(gemv_kernel<4, 2, 8>);
+        }
         return launch_status();
     }
     simt_linear_kernel<<<static_cast<unsigned>(blocks), kSimtWarps * 32, 0, s>>>(
