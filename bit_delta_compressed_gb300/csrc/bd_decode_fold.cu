@@ -33,19 +33,20 @@
 //     from HBM by TMA;
 //   * 3, the base issuer: per block four bf16 MMAs (N = pad16(M)) of the W
 //     tile with X_c; the only consumer of the W ring;
-//   * four issuer groups of five warps.  Group g owns the sign-accumulator
+//   * four issuer groups of six warps.  Group g owns the sign-accumulator
 //     columns of a contiguous run of 16-token chunks (balanced by the
 //     grouping kernel).  Its four expansion warps (one per tensor-memory lane
 //     quarter) turn the bits of the group's entries into e4m3 +-1 tiles in
 //     tensor memory (two buffers) -- one shift and one LOP3 per four weights:
 //     register j = ((w << (7 - j)) & 0x80808080) ^ 0xB8B8B8B8 holds columns
 //     j, j+8, j+16, j+24 of a 32-bit word -- and arrive on a named barrier;
-//     its issuer warp then issues, per 32-column K step, two e4m3 sign
+//     its two issuer warps then issue, per 32-column K step, two e4m3 sign
 //     products (hi, lo) per entry (a present variant with tokens in the
 //     group's columns; variant runs that share a chunk are separated by zero
-//     rows in X_p).  Groups write disjoint columns and need no ordering among
-//     themselves; the expansion warps finally read the group's columns of
-//     both accumulators and write y.
+//     rows in X_p), the entries dealt to them alternately: the issue rate of
+//     one warp, not the tensor core, bounds a step.  Groups and issuers write
+//     disjoint columns and need no ordering among themselves; the expansion
+//     warps finally read the group's columns of both accumulators and write y.
 // The columns inside each 32-column group of X_p are permuted to match the
 // register layout above.  MMAs are issued by converged warps (elect.sync).
 // Waiting warps poll with one lane that suspends in mbarrier.try_wait, and
@@ -66,7 +67,8 @@ constexpr int kWMax = 4;                        // W_base ring stages (runtime: 
 constexpr int kXMax = 2;                        // activation ring stages (runtime: 1 or 2)
 constexpr int kBStages = 2;                     // bits ring stages, two 64-column blocks each
 constexpr int kIss = kFoldIssuers;             // issuer groups
-constexpr int kGroupWarps = 5;                  // 4 expansion warps (one per lane quarter) + 1 issuer
+constexpr int kGroupIss = 2;                    // issuer warps per group (entries dealt alternately)
+constexpr int kGroupWarps = 4 + kGroupIss;      // 4 expansion warps (one per lane quarter) + the issuers
 constexpr int kBaseWarp = 3;                    // the base-product issuer
 constexpr int kFirstGroup = 4;                  // warps 0, 1, 2: W, activation and bits producers
 constexpr int kThreads = 32 * (kFirstGroup + kIss * kGroupWarps);
@@ -187,24 +189,28 @@ __device__ void base_issue(const FoldParams& p, uint32_t tmem, int nkb, uint8_t*
 // before the first step).  Every barrier is visited on every step, also
 // after an error, so the group never blocks.
 __device__ void group_issue(const FoldParams& p, const FoldPlan& fp, uint32_t tmem, uint32_t abase, int e0,
-                            int ne, int g, int nkb, uint8_t* xring, uint32_t xs_bytes, uint64_t* x_full,
+                            int ne, int g, int iss, int nkb, uint8_t* xring, uint32_t xs_bytes, uint64_t* x_full,
                             uint64_t* x_empty, uint64_t* ge, uint64_t* acc_full, uint64_t* drain) {
     using namespace sm100;
     const int lane = threadIdx.x & 31;
-    const bool work = ne > 0;
+    // this issuer's entries: e0 + iss, e0 + iss + kGroupIss, ... (their
+    // tiles sit at 8 (e - e0) columns inside the group's buffer of ne tiles)
+    const int own = ne > iss ? (ne - iss + kGroupIss - 1) / kGroupIss : 0;
+    const bool work = own > 0;
     const int Mb = p.Mb;
     // Operands of up to kRegEntries entries live in registers: the D column,
     // the low word of the B descriptor at stage 0 and step 0 (the stage and
     // step add 16-byte units to the start-address field; every address stays
     // below 256 KB, so the field never carries), and the instruction descriptor.
-    const bool in_regs = ne <= kRegEntries;
-    uint32_t r_d[kRegEntries], r_b[kRegEntries], r_id[kRegEntries];
+    const bool in_regs = own <= kRegEntries;
+    uint32_t r_d[kRegEntries], r_a[kRegEntries], r_b[kRegEntries], r_id[kRegEntries];
     const uint64_t xdesc = desc_sw128(smem_u32(xring));
     const uint32_t xdesc_lo = static_cast<uint32_t>(xdesc), xdesc_hi = static_cast<uint32_t>(xdesc >> 32);
 #pragma unroll
     for (int k = 0; k < kRegEntries; ++k) {
-        const int e = e0 + (k < ne ? k : 0);
+        const int e = e0 + (k < own ? iss + kGroupIss * k : 0);
         r_d[k] = tmem + kSCol0 + fp.e_col[e];
+        r_a[k] = static_cast<uint32_t>(8 * (e - e0));
         r_b[k] = xdesc_lo + static_cast<uint32_t>(Mb + fp.e_row[e]) * 8u;
         r_id[k] = idesc_e4m3(128, fp.e_n[e]);
     }
@@ -223,10 +229,10 @@ __device__ void group_issue(const FoldParams& p, const FoldPlan& fp, uint32_t tm
                 const uint32_t soff = (static_cast<uint32_t>(xs) * xs_bytes >> 4) + 2u * j;
 #pragma unroll
                 for (int k = 0; k < kRegEntries; ++k)
-                    if (k < ne) {
+                    if (k < own) {
                         const uint32_t blo = r_b[k] + soff;
-                        mma_e4m3_ts(r_d[k], abuf + 8 * k, (static_cast<uint64_t>(xdesc_hi) << 32) | blo, r_id[k]);
-                        mma_e4m3_ts(r_d[k], abuf + 8 * k, (static_cast<uint64_t>(xdesc_hi) << 32) | (blo + 4u), r_id[k]);
+                        mma_e4m3_ts(r_d[k], abuf + r_a[k], (static_cast<uint64_t>(xdesc_hi) << 32) | blo, r_id[k]);
+                        mma_e4m3_ts(r_d[k], abuf + r_a[k], (static_cast<uint64_t>(xdesc_hi) << 32) | (blo + 4u), r_id[k]);
                     }
                 commit_elect(&ge[j]);
                 if (j == 1) commit_elect(&x_empty[xs]);
@@ -234,7 +240,7 @@ __device__ void group_issue(const FoldParams& p, const FoldPlan& fp, uint32_t tm
                 tc_fence_after();
                 const uint32_t sxp = smem_u32(xring + xs * xs_bytes) + Mb * 128;
                 const uint32_t abuf = abase + j * 8 * ne;
-                for (int e = e0; e < e0 + ne; ++e) {
+                for (int e = e0 + iss; e < e0 + ne; e += kGroupIss) {
                     const uint32_t d = tmem + kSCol0 + fp.e_col[e];
                     const uint32_t a = abuf + 8 * (e - e0);
                     const uint32_t brow = sxp + fp.e_row[e] * 128 + 32 * j;
@@ -393,12 +399,12 @@ __global__ void __launch_bounds__(kThreads, 1) fold_decode_kernel(const __grid_c
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kWMax; ++s) { mbar_init(&w_full[s], 1); mbar_init(&w_empty[s], 1); }
-        for (int s = 0; s < kXMax; ++s) { mbar_init(&x_full[s], 1); mbar_init(&x_empty[s], kIss + 1); }
+        for (int s = 0; s < kXMax; ++s) { mbar_init(&x_full[s], 1); mbar_init(&x_empty[s], kIss * kGroupIss + 1); }
         for (int s = 0; s < kBStages; ++s) { mbar_init(&b_full[s], 1); mbar_init(&b_empty[s], 4 * kIss); }
         for (int g = 0; g < kIss; ++g)
-            for (int b = 0; b < kABufs; ++b) mbar_init(&g_empty[g][b], 1);
-        mbar_init(&acc_full, kIss + 1);
-        mbar_init(&drain, kIss + 1);
+            for (int b = 0; b < kABufs; ++b) mbar_init(&g_empty[g][b], kGroupIss);
+        mbar_init(&acc_full, kIss * kGroupIss + 1);
+        mbar_init(&drain, kIss * kGroupIss + 1);
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(&tmem_base, kTmemCols);
@@ -511,8 +517,8 @@ __global__ void __launch_bounds__(kThreads, 1) fold_decode_kernel(const __grid_c
         int a0 = 0;                                 // first +-1 tile column of this group
         for (int h = 0; h < g; ++h) a0 += 8 * kABufs * fp.iss_ne[h];
         const uint32_t abase = tmem + kACol0 + a0;
-        if (gw == kGroupWarps - 1)
-            group_issue(p, fp, tmem, abase, e0, ne, g, nkb, xring, xs_bytes, x_full, x_empty, g_empty[g], &acc_full,
+        if (gw >= 4)
+            group_issue(p, fp, tmem, abase, e0, ne, g, gw - 4, nkb, xring, xs_bytes, x_full, x_empty, g_empty[g], &acc_full,
                         &drain);
         else
             group_expand(p, pl, fp, tmem, abase, e0, ne, g, warp % 4, n0, nkb, g_empty[g], bring, bstage_bytes,
