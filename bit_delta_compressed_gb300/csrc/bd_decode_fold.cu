@@ -99,7 +99,7 @@ struct FoldParams {
     unsigned* diag;
     const uint8_t* ximg;                        // per 64-column block, the stage image of X_c and X_p
     int M, N, K, Mb, Rmax, splits, y_bf16;
-    int cluster_reduce;                         // the K slices of a row tile form one cluster (2..8 slices)
+    int cluster_reduce;                         // the K slices of a row tile form one cluster (2..16 slices)
     int wstages, xstages, bslots;               // ring depths; variants per bits stage
 };
 
@@ -828,7 +828,7 @@ int fold_rmax(int64_t M, int32_t V) {
     return r > 16 ? r : 16;
 }
 
-constexpr int kMaxClusterSplits = 8;           // portable cluster size
+constexpr int kMaxClusterSplits = 16;          // cluster size (above 8: non-portable, where the device allows it)
 
 // Clusters of `s` CTAs of the kernel (one per SM at `smem` bytes) that run at
 // once -- the GPCs' SM counts need not be multiples of s.  Cached per device;
@@ -839,6 +839,11 @@ int fold_cluster_capacity(int s, int smem) {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
     if (cache[dev][s] > 0) return cache[dev][s];
     if (!set_smem_attr(reinterpret_cast<const void*>(fold_decode_kernel), smem, 2)) return 0;
+    if (s > 8 && cudaFuncSetAttribute(reinterpret_cast<const void*>(fold_decode_kernel),
+                                      cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(s * 64));
     cfg.blockDim = dim3(kThreads);
@@ -860,7 +865,7 @@ int fold_cluster_capacity(int s, int smem) {
 
 // K slices per row tile (in pairs of 64-column blocks) and how they are
 // summed: minimise waves x (fixed per-CTA cost + blocks per slice x time per
-// block) + the split-K reduction.  Up to 8 slices may form one cluster and
+// block) + the split-K reduction.  Up to 16 slices may form one cluster and
 // be summed in shared memory (waves counted in the clusters that fit at
 // once, the reduction nearly free); otherwise the CTA that finishes the tile
 // last sums the slices' partials from HBM, with waves counted in single CTAs
