@@ -23,8 +23,10 @@
 // tiles, and the scale is applied per column (and row) in the epilogue.
 //
 // One CTA owns 128 output rows (the 128 lanes of tensor memory) and a slice
-// of K (split-K at even 64-column blocks, summed in a fixed order by the CTA
-// that finishes the tile last).  Warps:
+// of K (split-K at even 64-column blocks; the slices of a row tile are summed
+// in a fixed order, over the shared memory of a thread-block cluster of up to
+// 16 CTAs, or from HBM partials by the CTA that finishes the tile last).
+// Warps:
 //   * 0, 1, 2 (producers, each with a ring of its own): W_base tiles
 //     (128 x 64 bf16, 128-byte swizzle) from HBM by TMA; per 64-column block
 //     the scaled activations X_c (pad16(M) rows) and the sign operand X_p (R
