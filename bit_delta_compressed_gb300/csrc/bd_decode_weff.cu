@@ -159,6 +159,27 @@ __global__ void __launch_bounds__(kThreads, 1) weff_decode_kernel(const __grid_c
         mbar_init(&acc_full, 1);
         fence_mbar_init();
     }
+    // the producer (thread 0, which initialised the barriers) issues the
+    // first stages at once; the tensor-memory allocation and the block
+    // barrier below overlap their flight
+    const uint32_t tx = kWTile + static_cast<uint32_t>(Mb) * 128u;
+    const int early = nkb < kStages ? nkb : kStages;
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&p.tm_w);
+        prefetch_tensormap(&p.tm_x);
+        prefetch_tensormap(&p.tm_bits);
+        for (int i = 0; i < early; ++i) {
+            if ((i & 1) == 0) {
+                const int bs = (i >> 1) & 1;
+                mbar_expect_tx(&b_full[bs], 2048u);
+                tma_load_2d(bring + bs * 2048, &p.tm_bits, &b_full[bs], 2 * (kb0 + i), n0);
+            }
+            uint8_t* st = base + i * sbytes;
+            mbar_expect_tx(&full[i], tx);
+            tma_load_2d(st, &p.tm_w, &full[i], (kb0 + i) * kBK, n0);
+            tma_load_2d(st + 2 * kWTile, &p.tm_x, &full[i], (kb0 + i) * kBK, 0);
+        }
+    }
     if (warp == 1) tmem_alloc(&tmem_base, kTmemCols);
     tc_fence_before();
     __syncthreads();
@@ -168,12 +189,8 @@ __global__ void __launch_bounds__(kThreads, 1) weff_decode_kernel(const __grid_c
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
-            prefetch_tensormap(&p.tm_w);
-            prefetch_tensormap(&p.tm_x);
-            prefetch_tensormap(&p.tm_bits);
-            const uint32_t tx = kWTile + static_cast<uint32_t>(Mb) * 128u;
-            int issued = 0, bissued = 0;
-            for (int i = 0; i < nkb; ++i) {
+            int issued = early, bissued = (early + 1) / 2;
+            for (int i = early; i < nkb; ++i) {
                 const int s = i % kStages;
                 if ((i & 1) == 0) {
                     const int m = i >> 1, bs = m & 1;
