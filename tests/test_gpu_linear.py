@@ -292,3 +292,22 @@ def test_small_batch_cuda_cores(bd, o, M, N, K, V, per_row):
     ref = o.linear(bf16_np(x)[good], ids_h[good], bf16_np(wb), f32_np(alphas), [bits_np(b) for b in bits],
                    rows=rows, per_row_alpha=per_row)
     assert_y_close(y[good][:, rows], ref, "cuda cores M=%d N=%d K=%d V=%d rows=%s" % (M, N, K, V, per_row))
+
+
+@pytest.mark.parametrize("N,K,M", [(200, 8192, 128), (1000, 8192, 64), (1366, 16384, 16), (2048, 4096, 128),
+                                   (1024, 28672, 32)])
+def test_folded_split_reductions(bd, o, N, K, M):
+    """The folded kernel's K slices summed over a cluster's shared memory (2 to
+    16 slices) or through HBM partials, on ragged row counts (a partial last
+    row tile) and deep K: every output row against the oracle."""
+    g = wl.generator(990 + M + N // 100, DEV)
+    V = 14
+    wb = wl.base_weights(N, K, g, DEV)
+    bits = random_bits(g, N, K, V)
+    alphas = 2e-4 + 1.8e-3 * torch.rand(V, generator=g, device=DEV)
+    x = wl.activations(M, K, g, DEV)
+    ids = wl.variant_ids_zipf(M, V, 1.1, wl.generator(991)).to(DEV)
+    ids[::9] = -1
+    y = run(bd, "decode_fold", x, ids, wb, alphas, bits, out_dtype=torch.bfloat16)
+    ref = oracle_y(o, x, ids, wb, alphas, bits)
+    assert_y_close(y, ref, "folded splits N=%d K=%d M=%d" % (N, K, M))
