@@ -35,20 +35,23 @@
 //     from HBM by TMA;
 //   * 3, the base issuer: per block four bf16 MMAs (N = pad16(M)) of the W
 //     tile with X_c; the only consumer of the W ring;
-//   * four issuer groups of six warps.  Group g owns the sign-accumulator
-//     columns of a contiguous run of 16-token chunks (balanced by the
-//     grouping kernel).  Its four expansion warps (one per tensor-memory lane
-//     quarter) turn the bits of the group's entries into e4m3 +-1 tiles in
-//     tensor memory (two buffers) -- one shift and one LOP3 per four weights:
-//     register j = ((w << (7 - j)) & 0x80808080) ^ 0xB8B8B8B8 holds columns
-//     j, j+8, j+16, j+24 of a 32-bit word -- and arrive on a named barrier;
-//     its two issuer warps then issue, per 32-column K step, two e4m3 sign
-//     products (hi, lo) per entry (a present variant with tokens in the
-//     group's columns; variant runs that share a chunk are separated by zero
-//     rows in X_p), the entries dealt to them alternately: the issue rate of
-//     one warp, not the tensor core, bounds a step.  Groups and issuers write
-//     disjoint columns and need no ordering among themselves; the expansion
-//     warps finally read the group's columns of both accumulators and write y.
+//   * four issuer groups of six warps.  An entry is one present variant
+//     (its run of grouped positions, the 16-token chunks it touches and its
+//     rows of X_p; variant runs that share a chunk are separated by zero rows
+//     in X_p); entry e belongs to group e % 4, so the groups' loads differ by
+//     one entry at most.  A group's four expansion warps (one per
+//     tensor-memory lane quarter) turn the bits of its entries into e4m3 +-1
+//     tiles in tensor memory (two buffers) -- one shift and one LOP3 per four
+//     weights: register j = ((w << (7 - j)) & 0x80808080) ^ 0xB8B8B8B8 holds
+//     columns j, j+8, j+16, j+24 of a 32-bit word -- and arrive on a named
+//     barrier; its two issuer warps then issue, per 32-column K step, two
+//     e4m3 sign products (hi, lo) per entry, the entries dealt to them
+//     alternately: the issue rate of a warp, not the tensor core, bounds a
+//     step.  Entries of different groups may add into the same accumulator
+//     columns (each MMA's accumulation is atomic in the tensor pipe), so all
+//     sign columns are zeroed before the first sign product; at the end each
+//     group's expansion warps read a quarter of the columns of both
+//     accumulators and write y.
 // The columns inside each 32-column group of X_p are permuted to match the
 // register layout above.  MMAs are issued by converged warps (elect.sync).
 // Waiting warps poll with one lane that suspends in mbarrier.try_wait, and
@@ -217,11 +220,12 @@ __device__ void base_issue(const FoldParams& p, uint32_t tmem, int nkb, uint8_t*
 // after an error, so the group never blocks.
 __device__ void group_issue(const FoldParams& p, const FoldPlan& fp, uint32_t tmem, uint32_t abase, int e0,
                             int ne, int g, int iss, int nkb, uint8_t* xring, uint32_t xs_bytes, uint64_t* x_full,
-                            uint64_t* x_empty, uint64_t* ge, uint64_t* acc_full, uint64_t* drain) {
+                            uint64_t* x_empty, uint64_t* ge, uint64_t* zeroed, uint64_t* acc_full, uint64_t* drain) {
     using namespace sm100;
     const int lane = threadIdx.x & 31;
-    // this issuer's entries: e0 + iss, e0 + iss + kGroupIss, ... (their
-    // tiles sit at 8 (e - e0) columns inside the group's buffer of ne tiles)
+    // The group's entries are e0 + kIss l, l = 0 .. ne - 1 (tile of entry l at
+    // 8 l columns inside the group's buffer of ne tiles); this issuer takes
+    // l = iss, iss + kGroupIss, ...
     const int own = ne > iss ? (ne - iss + kGroupIss - 1) / kGroupIss : 0;
     const bool work = own > 0;
     const int Mb = p.Mb;
@@ -235,13 +239,16 @@ __device__ void group_issue(const FoldParams& p, const FoldPlan& fp, uint32_t tm
     const uint32_t xdesc_lo = static_cast<uint32_t>(xdesc), xdesc_hi = static_cast<uint32_t>(xdesc >> 32);
 #pragma unroll
     for (int k = 0; k < kRegEntries; ++k) {
-        const int e = e0 + (k < own ? iss + kGroupIss * k : 0);
+        const int l = k < own ? iss + kGroupIss * k : 0;
+        const int e = e0 + kIss * l;
         r_d[k] = tmem + kSCol0 + fp.e_col[e];
-        r_a[k] = static_cast<uint32_t>(8 * (e - e0));
+        r_a[k] = static_cast<uint32_t>(8 * l);
         r_b[k] = xdesc_lo + static_cast<uint32_t>(Mb + fp.e_row[e]) * 8u;
         r_id[k] = idesc_e4m3(128, fp.e_n[e]);
     }
-    bool ok = true;
+    // entries of every group may share accumulator columns: all of them are
+    // zeroed before the first sign product
+    bool ok = warp_wait(zeroed, 0, kWaitLimit, p.status, 34, p.diag);
     for (int i = 0; i < nkb; ++i) {
         const int xs = i % p.xstages;
         for (int j = 0; j < 2; ++j) {
@@ -267,9 +274,10 @@ __device__ void group_issue(const FoldParams& p, const FoldPlan& fp, uint32_t tm
                 tc_fence_after();
                 const uint32_t sxp = smem_u32(xring + xs * xs_bytes) + Mb * 128;
                 const uint32_t abuf = abase + j * 8 * ne;
-                for (int e = e0 + iss; e < e0 + ne; e += kGroupIss) {
+                for (int l = iss; l < ne; l += kGroupIss) {
+                    const int e = e0 + kIss * l;
                     const uint32_t d = tmem + kSCol0 + fp.e_col[e];
-                    const uint32_t a = abuf + 8 * (e - e0);
+                    const uint32_t a = abuf + 8 * l;
                     const uint32_t brow = sxp + fp.e_row[e] * 128 + 32 * j;
                     const uint32_t id8 = idesc_e4m3(128, fp.e_n[e]);
                     mma_e4m3_ts(d, a, desc_sw128(brow), id8);
@@ -314,7 +322,7 @@ __device__ __forceinline__ void store_signs(uint32_t taddr, uint32_t w) {
 __device__ void group_expand(const FoldParams& p, const SegPlan& pl, const FoldPlan& fp, uint32_t tmem,
                              uint32_t abase, int e0, int ne, int g, int q4, int n0, int nkb, uint64_t* ge,
                              const uint8_t* bring, uint32_t bstage_bytes, uint64_t* b_full, uint64_t* b_empty,
-                             uint64_t* acc_full, const int32_t* tok_s, const float* scale_s, const int32_t* var_s,
+                             uint64_t* zeroed, uint64_t* acc_full, const int32_t* tok_s, const float* scale_s, const int32_t* var_s,
                              const float* alpha_s, int split, int bcol, int bn, float* psm) {
     using namespace sm100;
     const int lane = threadIdx.x & 31;
@@ -329,6 +337,9 @@ __device__ void group_expand(const FoldParams& p, const SegPlan& pl, const FoldP
         for (int jj = 0; jj < 8; ++jj) z[jj] = 0u;
         for (int c = bcol; c < bcol + bn; c += 8) tmem_st8(tmem + lane_addr + kSCol0 + c, z);
         tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(zeroed);
     }
     bool ok = true;
     for (int i = 0; i < nkb; ++i) {
@@ -340,18 +351,9 @@ __device__ void group_expand(const FoldParams& p, const SegPlan& pl, const FoldP
             if (ok) {
                 tc_fence_after();
                 const uint32_t col = abase + lane_addr + j * 8 * ne;
-                int k = 0;
-                for (; k + 4 <= ne; k += 4) {           // four tiles per tensor-memory store
-                    uint32_t v[32];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint32_t w = words[fp.e_slot[e0 + k + q] * 512 + j];
-#pragma unroll
-                        for (int jj = 0; jj < 8; ++jj) v[8 * q + jj] = ((w << (7 - jj)) & 0x80808080u) ^ 0xB8B8B8B8u;
-                    }
-                    tmem_st32(col + 8 * k, v);
-                }
-                for (; k < ne; ++k) store_signs(col + 8 * k, words[fp.e_slot[e0 + k] * 512 + j]);
+                // one 8-column store per tile: a warp writes its 32 lanes of
+                // four tiles faster as four such stores than as one 32-column store
+                for (int k = 0; k < ne; ++k) store_signs(col + 8 * k, words[fp.e_slot[e0 + kIss * k] * 512 + j]);
                 tmem_st_wait();
             }
             tc_fence_before();
@@ -397,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1) fold_decode_kernel(const __grid_c
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
     __shared__ uint64_t w_full[kWMax], w_empty[kWMax], x_full[kXMax], x_empty[kXMax];
     __shared__ uint64_t b_full[kBStages], b_empty[kBStages];
-    __shared__ uint64_t g_empty[kIss][kABufs], acc_full, drain;
+    __shared__ uint64_t g_empty[kIss][kABufs], zeroed, acc_full, drain;
     __shared__ uint32_t tmem_base;
     __shared__ SegPlan pl;
     __shared__ FoldPlan fp;
@@ -430,6 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1) fold_decode_kernel(const __grid_c
         for (int s = 0; s < kBStages; ++s) { mbar_init(&b_full[s], 1); mbar_init(&b_empty[s], 4 * kIss); }
         for (int g = 0; g < kIss; ++g)
             for (int b = 0; b < kABufs; ++b) mbar_init(&g_empty[g][b], kGroupIss);
+        mbar_init(&zeroed, 4 * kIss);
         mbar_init(&acc_full, kIss * kGroupIss + 1);
         mbar_init(&drain, kIss * kGroupIss + 1);
         fence_mbar_init();
@@ -545,11 +548,11 @@ __global__ void __launch_bounds__(kThreads, 1) fold_decode_kernel(const __grid_c
         for (int h = 0; h < g; ++h) a0 += 8 * kABufs * fp.iss_ne[h];
         const uint32_t abase = tmem + kACol0 + a0;
         if (gw >= 4)
-            group_issue(p, fp, tmem, abase, e0, ne, g, gw - 4, nkb, xring, xs_bytes, x_full, x_empty, g_empty[g], &acc_full,
-                        &drain);
+            group_issue(p, fp, tmem, abase, e0, ne, g, gw - 4, nkb, xring, xs_bytes, x_full, x_empty, g_empty[g], &zeroed,
+                        &acc_full, &drain);
         else
             group_expand(p, pl, fp, tmem, abase, e0, ne, g, warp % 4, n0, nkb, g_empty[g], bring, bstage_bytes,
-                         b_full, b_empty, &acc_full, tok_s, scale_s, var_s, alpha_s, split, bcol, bn,
+                         b_full, b_empty, &zeroed, &acc_full, tok_s, scale_s, var_s, alpha_s, split, bcol, bn,
                          reinterpret_cast<float*>(base));
     }
 

@@ -79,16 +79,17 @@ struct SegPlan {
 
 // Issue plan of the folded tensor-core decode kernel, also written by the
 // grouping kernel.  The accumulator has one column per grouped position
-// (pad16(M) columns, 16-column chunks); issuer warp i owns the chunk range
-// [iss_col[i], iss_col[i] + iss_n[i]) and issues, per K step, the base
-// product over its range plus one "entry" per present variant whose tokens
-// fall inside it.  Entry e covers columns [e_col, e_col + e_n) with rows
-// [e_row, e_row + e_n) of the sign operand (rows of other variants' tokens
-// are zero there) and the +-1 tile of present variant e_slot.  The base
-// product (all columns at once) has an issuer of its own.
+// (pad16(M) columns, 16-column chunks).  Entry e is present variant e_slot
+// (one run of grouped positions): it covers columns [e_col, e_col + e_n)
+// with rows [e_row, e_row + e_n) of the sign operand (rows of other
+// variants' tokens are zero there) and the +-1 tile of that variant.  Issuer
+// group i expands and issues entries iss_e0[i], iss_e0[i] + kFoldIssuers, ...
+// (iss_ne[i] of them), and zeroes and writes out the columns [iss_col[i],
+// iss_col[i] + iss_n[i]).  The base product (all columns at once) has an
+// issuer of its own.
 constexpr int kFoldIssuers = 4;
 constexpr int kFoldMaxSlots = 16;                       // present variants
-constexpr int kFoldMaxEntries = kFoldMaxSlots + kFoldIssuers;
+constexpr int kFoldMaxEntries = kFoldMaxSlots;          // one entry per present variant
 constexpr int kFoldMaxCols = 128;                       // pad16(M)
 constexpr int kFoldSepEntries = 16;                     // entries whose +-1 tiles fit (two buffers)
 struct FoldPlan {

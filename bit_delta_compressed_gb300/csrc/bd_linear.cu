@@ -56,14 +56,14 @@ __device__ __forceinline__ int bucket_of(int32_t id, int V) {
     return (id >= -1 && id < V) ? id + 1 : V + 1;
 }
 
-// Issue plan of the folded decode kernel.  The 16-column chunks of the sign
-// accumulator are cut into at most kFoldIssuers contiguous ranges so that
-// the largest per-range entry count -- one entry (two sign MMAs, hi and lo,
-// per K step) per variant run touching the range -- is as small as possible
-// (a tiny dynamic programme over at most 8 chunks).  A run cut by a range
-// boundary costs an extra entry; when the entries would not fit the
-// kernel's +-1 tile buffers (kFoldSepEntries), fewer ranges are used (one
-// range always fits).
+// Issue plan of the folded decode kernel.  Each present variant's run of
+// grouped positions is one "entry": its +-1 tile, two sign MMAs (hi, lo) per
+// K step over the 16-column chunks the run touches, and those chunks' rows
+// of the sign operand.  The entries are dealt to the kFoldIssuers issuer
+// groups round-robin (entry e to group e % kFoldIssuers), so no group has
+// more than one entry above another whatever the run lengths; the chunks
+// are split into kFoldIssuers near-equal contiguous ranges only for zeroing
+// the sign accumulator and for the epilogue.
 constexpr int kFoldChunks = kFoldMaxCols / 16;
 
 // Bit d of mask[c]: run d (first position off[d], cnt[d] tokens) has a token
@@ -76,45 +76,6 @@ __device__ void fold_masks(const int32_t* off, const int32_t* cnt, int D, uint32
     }
 }
 
-// Range boundaries bnd[0..kFoldIssuers] over C chunks; returns the busiest
-// range's entry count.
-__device__ int fold_ranges(const uint32_t* mask, int C, int* bnd) {
-    constexpr int I = kFoldIssuers, CM = kFoldChunks;
-    int cst[CM + 1][CM + 1];                      // entries of chunk range [a, b)
-    for (int a = 0; a <= C; ++a) {
-        uint32_t m = 0;
-        cst[a][a] = 0;
-        for (int b = a + 1; b <= C; ++b) { m |= mask[b - 1]; cst[a][b] = __popc(m); }
-    }
-    constexpr int kBig = 1 << 20;
-    int worst = 0;
-    for (int G = I; G >= 1; --G) {
-        int f[I + 1][CM + 1], arg[I + 1][CM + 1];
-        for (int c = 0; c <= C; ++c) { f[0][c] = c == 0 ? 0 : kBig; arg[0][c] = 0; }
-        for (int i = 1; i <= G; ++i)
-            for (int c = 0; c <= C; ++c) {
-                int best = kBig, ba = 0;
-                for (int a = 0; a <= c; ++a) {
-                    const int v = max(f[i - 1][a], cst[a][c]);
-                    if (v < best) { best = v; ba = a; }
-                }
-                f[i][c] = best;
-                arg[i][c] = ba;
-            }
-        for (int i = G + 1; i <= I; ++i) bnd[i] = C;
-        bnd[G] = C;
-        for (int i = G; i >= 1; --i) bnd[i - 1] = arg[i][bnd[i]];
-        int entries = 0;
-        worst = 0;
-        for (int i = 0; i < G; ++i) {
-            entries += cst[bnd[i]][bnd[i + 1]];
-            worst = max(worst, cst[bnd[i]][bnd[i + 1]]);
-        }
-        if (entries <= kFoldSepEntries) break;
-    }
-    return worst;
-}
-
 __device__ void fold_plan(const SegPlan& pl, int M, FoldPlan* fp) {
     constexpr int I = kFoldIssuers;
     const int C = pad16(M) / 16;
@@ -124,30 +85,23 @@ __device__ void fold_plan(const SegPlan& pl, int M, FoldPlan* fp) {
     fp->n_entries = 0;
     for (int i = 0; i < I; ++i) { fp->iss_col[i] = 0; fp->iss_n[i] = 0; fp->iss_e0[i] = 0; fp->iss_ne[i] = 0; }
     if (C > kFoldChunks || pl.D > kFoldMaxSlots) return;
-    uint32_t mask[kFoldChunks];
-    fold_masks(pl.off, pl.cnt, pl.D, mask);
-    int bnd[I + 1];
-    fold_ranges(mask, C, bnd);
-    int e = 0, row = 0;
+    int row = 0;
+    for (int d = 0; d < pl.D; ++d) {
+        const int c0 = pl.off[d] / 16, c1 = (pl.off[d] + pl.cnt[d] - 1) / 16;
+        fp->e_col[d] = 16 * c0;
+        fp->e_n[d] = 16 * (c1 - c0 + 1);
+        fp->e_slot[d] = d;
+        fp->e_row[d] = row;
+        row += 16 * (c1 - c0 + 1);
+    }
     for (int i = 0; i < I; ++i) {
-        const int a = bnd[i], b = bnd[i + 1];
+        const int a = C * i / I, b = C * (i + 1) / I;
         fp->iss_col[i] = 16 * a;
         fp->iss_n[i] = 16 * (b - a);
-        fp->iss_e0[i] = e;
-        for (int d = 0; d < pl.D && b > a; ++d) {
-            const int c0 = pl.off[d] / 16, c1 = (pl.off[d] + pl.cnt[d] - 1) / 16;
-            const int cs = max(c0, a), ce = min(c1, b - 1);
-            if (cs > ce) continue;
-            fp->e_col[e] = 16 * cs;
-            fp->e_n[e] = 16 * (ce - cs + 1);
-            fp->e_slot[e] = d;
-            fp->e_row[e] = row;
-            row += 16 * (ce - cs + 1);
-            ++e;
-        }
-        fp->iss_ne[i] = e - fp->iss_e0[i];
+        fp->iss_e0[i] = i;                              // entries i, i + I, i + 2 I, ...
+        fp->iss_ne[i] = pl.D > i ? (pl.D - i + I - 1) / I : 0;
     }
-    fp->n_entries = e;
+    fp->n_entries = pl.D;
     fp->R = row;
     fp->ok = 1;
 }
@@ -176,9 +130,9 @@ __device__ void run_order(int cand, const int* present, int D, int* ord) {
     }
 }
 
-// Score of an order for the folded kernel: busiest issuer's entries first,
-// then the sign-operand rows (in chunks).
-__device__ int order_score(const int* ord, int D, const int* total, int n_base, int C) {
+// Score of an order for the folded kernel: the sign-operand rows (in
+// chunks) -- runs that share a chunk each need its rows.
+__device__ int order_score(const int* ord, int D, const int* total, int n_base) {
     int32_t off[kFoldMaxSlots], cnt[kFoldMaxSlots];
     int run = n_base;
     for (int d = 0; d < D; ++d) {
@@ -188,11 +142,9 @@ __device__ int order_score(const int* ord, int D, const int* total, int n_base, 
     }
     uint32_t mask[kFoldChunks];
     fold_masks(off, cnt, D, mask);
-    int bnd[kFoldIssuers + 1];
-    const int worst = fold_ranges(mask, C, bnd);
     int rows = 0;
-    for (int c = 0; c < C; ++c) rows += __popc(mask[c]);
-    return worst * 256 + rows;
+    for (int c = 0; c < kFoldChunks; ++c) rows += __popc(mask[c]);
+    return rows;
 }
 
 __global__ void __launch_bounds__(1024) group_kernel(const int32_t* __restrict__ ids, int M, int V,
@@ -235,7 +187,7 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t* __restrict__
             const int cand = threadIdx.x * kOrderTries + k;
             int ord[kFoldMaxSlots];
             run_order(cand, present, D, ord);
-            const unsigned long long kk = (static_cast<unsigned long long>(order_score(ord, D, total, total[0], C)) << 32) |
+            const unsigned long long kk = (static_cast<unsigned long long>(order_score(ord, D, total, total[0])) << 32) |
                                           static_cast<unsigned>(cand);
             key = kk < key ? kk : key;
         }
