@@ -319,7 +319,7 @@ __device__ __forceinline__ void store_signs(uint32_t taddr, uint32_t w) {
 // words per present variant, two 64-column blocks per stage), and arrive on
 // the group's named barrier; at the end read the group's accumulator columns
 // and write y = 2^-s_t D.
-__device__ void group_expand(const FoldParams& p, const SegPlan& pl, const FoldPlan& fp, uint32_t tmem,
+__device__ void group_expand(const FoldParams& p, const FoldPlan& fp, uint32_t tmem,
                              uint32_t abase, int e0, int ne, int g, int q4, int n0, int nkb, uint64_t* ge,
                              const uint8_t* bring, uint32_t bstage_bytes, uint64_t* b_full, uint64_t* b_empty,
                              uint64_t* zeroed, uint64_t* acc_full, const int32_t* tok_s, const float* scale_s, const int32_t* var_s,
@@ -369,25 +369,45 @@ __device__ void group_expand(const FoldParams& p, const SegPlan& pl, const FoldP
     if (ok) ok = warp_wait(acc_full, 0, kWaitLimit, p.status, 29, p.diag);
     if (!ok) return;
     tc_fence_after();
-    const int n_valid = pl.M - pl.n_invalid;
     for (int c0 = bcol; c0 < bcol + bn; c0 += 16) {
         uint32_t v[16], u[16];
         tmem_ld16(tmem + lane_addr + c0, v);
         tmem_ld16(tmem + lane_addr + kSCol0 + c0, u);
+        // the chunk's coefficients, the same for every lane: broadcast loads,
+        // eight positions at a time, the first eight issued before the wait
+        // on the tensor-memory loads
+        float a[8], sc[8];
+        auto coefs = [&](int t0) {
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const float4 a4 = reinterpret_cast<const float4*>(alpha_s + c0 + t0)[q];
+                const float4 s4 = reinterpret_cast<const float4*>(scale_s + c0 + t0)[q];
+                a[4 * q] = a4.x; a[4 * q + 1] = a4.y; a[4 * q + 2] = a4.z; a[4 * q + 3] = a4.w;
+                sc[4 * q] = s4.x; sc[4 * q + 1] = s4.y; sc[4 * q + 2] = s4.z; sc[4 * q + 3] = s4.w;
+            }
+            if (p.alpha_rows && row_ok) {
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    const int vv = var_s[c0 + t0 + t];
+                    a[t] = vv >= 0 ? __ldg(p.alphas + static_cast<int64_t>(vv) * p.N + n) : 0.f;
+                }
+            }
+        };
+        coefs(0);
         tmem_ld_wait();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            if (h == 1) coefs(8);
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+                v[8 * h + t] = __float_as_uint(fmaf(a[t], __uint_as_float(u[8 * h + t]), __uint_as_float(v[8 * h + t])) * sc[t]);
+        }
         if (row_ok) {
 #pragma unroll
             for (int t = 0; t < 16; ++t) {
                 const int pos = c0 + t;
-                if (pos >= p.M) break;
-                const int vv = var_s[pos];
-                float d = __uint_as_float(v[t]);
-                if (vv >= 0) {
-                    const float a = p.alpha_rows ? __ldg(p.alphas + static_cast<int64_t>(vv) * p.N + n) : alpha_s[pos];
-                    d = fmaf(a, __uint_as_float(u[t]), d);
-                }
-                const float val = pos < n_valid ? d * scale_s[pos] : 0.f;
-                store_out(p, psm, split, pos, tok_s[pos], n, r, val);
+                const float val = __uint_as_float(v[t]);
+                if (pos < p.M) store_out(p, psm, split, pos, tok_s[pos], n, r, val);
             }
         }
     }
@@ -405,9 +425,9 @@ __global__ void __launch_bounds__(kThreads, 1) fold_decode_kernel(const __grid_c
     __shared__ FoldPlan fp;
     __shared__ int last_cta;
     __shared__ int32_t tok_s[kFoldMaxCols];
-    __shared__ float scale_s[kFoldMaxCols];
+    __shared__ __align__(16) float scale_s[kFoldMaxCols];   // 2^-s_t, 0 for invalid and padding positions
     __shared__ int32_t var_s[kFoldMaxCols];
-    __shared__ float alpha_s[kFoldMaxCols];      // per-matrix scale of the position's variant
+    __shared__ __align__(16) float alpha_s[kFoldMaxCols];   // per-matrix scale of the position's variant, 0 for base
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Mb = p.Mb;
@@ -450,8 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1) fold_decode_kernel(const __grid_c
     }
     for (int q = threadIdx.x; q < Mb; q += blockDim.x) {
         tok_s[q] = q < p.M ? p.pos2tok[q] : -1;
-        scale_s[q] = pow2i(-p.sexp[q]);
         var_s[q] = q < p.M ? p.pos_var[q] : -2;
+        scale_s[q] = var_s[q] == -2 ? 0.f : pow2i(-p.sexp[q]);
         alpha_s[q] = (!p.alpha_rows && var_s[q] >= 0) ? p.alphas[var_s[q]] : 0.f;
     }
     tc_fence_before();
@@ -551,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1) fold_decode_kernel(const __grid_c
             group_issue(p, fp, tmem, abase, e0, ne, g, gw - 4, nkb, xring, xs_bytes, x_full, x_empty, g_empty[g], &zeroed,
                         &acc_full, &drain);
         else
-            group_expand(p, pl, fp, tmem, abase, e0, ne, g, warp % 4, n0, nkb, g_empty[g], bring, bstage_bytes,
+            group_expand(p, fp, tmem, abase, e0, ne, g, warp % 4, n0, nkb, g_empty[g], bring, bstage_bytes,
                          b_full, b_empty, &zeroed, &acc_full, tok_s, scale_s, var_s, alpha_s, split, bcol, bn,
                          reinterpret_cast<float*>(base));
     }
@@ -570,29 +590,58 @@ __global__ void __launch_bounds__(kThreads, 1) fold_decode_kernel(const __grid_c
         const int total = p.M * per_t;
         const int g0 = static_cast<int>(static_cast<int64_t>(split) * total / p.splits);
         const int g1 = static_cast<int>(static_cast<int64_t>(split + 1) * total / p.splits);
-        for (int gi = g0 + static_cast<int>(threadIdx.x); gi < g1; gi += blockDim.x) {
-            const int pos = gi / per_t, r4 = 4 * (gi % per_t);
-            if (r4 >= rows) continue;
-            const uint32_t off = psm_a + static_cast<uint32_t>(gi) * 16u;
-            float4 acc = ld_cluster_f4(cluster_map(off, 0));
-            for (int sl = 1; sl < p.splits; ++sl) {
-                const float4 a = ld_cluster_f4(cluster_map(off, static_cast<uint32_t>(sl)));
-                acc.x += a.x; acc.y += a.y; acc.z += a.z; acc.w += a.w;
+        // two float4 groups per thread and pass, the slices read four at a
+        // time before they are added (in order): the remote loads of a pass
+        // are in flight together
+        const int nt = static_cast<int>(blockDim.x);
+        for (int gb = g0 + static_cast<int>(threadIdx.x); gb < g1; gb += 2 * nt) {
+            const int gq[2] = {gb, gb + nt};
+            float4 acc[2];
+            bool live[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                live[h] = gq[h] < g1 && 4 * (gq[h] % per_t) < rows;
+                acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (live[h]) acc[h] = ld_cluster_f4(cluster_map(psm_a + static_cast<uint32_t>(gq[h]) * 16u, 0));
             }
-            const int64_t o = static_cast<int64_t>(tok_s[pos]) * p.N + n0 + r4;
-            if (r4 + 4 <= rows && (p.N & 3) == 0) {
-                if (p.y_bf16) {
-                    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
-                    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.y) + o) =
-                        make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+            for (int sl = 1; sl < p.splits; sl += 4) {
+                float4 part[2][4];
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (live[h] && sl + q < p.splits)
+                            part[h][q] = ld_cluster_f4(cluster_map(psm_a + static_cast<uint32_t>(gq[h]) * 16u,
+                                                                   static_cast<uint32_t>(sl + q)));
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (live[h] && sl + q < p.splits) {
+                            acc[h].x += part[h][q].x; acc[h].y += part[h][q].y;
+                            acc[h].z += part[h][q].z; acc[h].w += part[h][q].w;
+                        }
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (!live[h]) continue;
+                const int pos = gq[h] / per_t, r4 = 4 * (gq[h] % per_t);
+                const int64_t o = static_cast<int64_t>(tok_s[pos]) * p.N + n0 + r4;
+                const float4 a = acc[h];
+                if (r4 + 4 <= rows && (p.N & 3) == 0) {
+                    if (p.y_bf16) {
+                        const __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y), hi = __floats2bfloat162_rn(a.z, a.w);
+                        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.y) + o) =
+                            make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+                    } else {
+                        *reinterpret_cast<float4*>(static_cast<float*>(p.y) + o) = a;
+                    }
                 } else {
-                    *reinterpret_cast<float4*>(static_cast<float*>(p.y) + o) = acc;
-                }
-            } else {
-                const float v4[4] = {acc.x, acc.y, acc.z, acc.w};
-                for (int j = 0; j < 4 && r4 + j < rows; ++j) {
-                    if (p.y_bf16) static_cast<__nv_bfloat16*>(p.y)[o + j] = __float2bfloat16_rn(v4[j]);
-                    else static_cast<float*>(p.y)[o + j] = v4[j];
+                    const float v4[4] = {a.x, a.y, a.z, a.w};
+                    for (int j = 0; j < 4 && r4 + j < rows; ++j) {
+                        if (p.y_bf16) static_cast<__nv_bfloat16*>(p.y)[o + j] = __float2bfloat16_rn(v4[j]);
+                        else static_cast<float*>(p.y)[o + j] = v4[j];
+                    }
                 }
             }
         }
