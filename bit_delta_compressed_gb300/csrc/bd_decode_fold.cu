@@ -53,7 +53,9 @@
 //     group's expansion warps read a quarter of the columns of both
 //     accumulators and write y.
 // The columns inside each 32-column group of X_p are permuted to match the
-// register layout above.  MMAs are issued by converged warps (elect.sync).
+// register layout above.  One elected lane of an issuer warp issues all of
+// its MMAs and commits of a step in a row (an elect per MMA by the whole warp
+// costs ~6% of the kernel's time, and a plain lane-0 branch far more).
 // Waiting warps poll with one lane that suspends in mbarrier.try_wait, and
 // the sign bits come by TMA: per-thread global loads or polling by whole
 // warps slow the tensor-core issue of the whole SM.
@@ -112,32 +114,12 @@ __device__ __forceinline__ float pow2i(int e) {        // exact 2^e, e in [-126,
     return __int_as_float((127 + e) << 23);
 }
 
-// tcgen05.mma issued by one elected lane of a converged warp.
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-__device__ __forceinline__ void mma_e4m3_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc) {
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "setp.ne.b32 p, 1, 0;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
-        "r"(a_tmem), "l"(b), "r"(idesc)
-        : "memory");
-}
-__device__ __forceinline__ void commit_elect(uint64_t* bar) {
-    asm volatile(
-        "{\n\t.reg .pred e;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
-            sm100::smem_u32(bar))
-        : "memory");
+// True in one lane of a converged warp (the lowest): the lane that issues the
+// warp's MMAs and commits, so that each commit tracks that lane's MMAs.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t e;
+    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(e));
+    return e != 0;
 }
 
 // Output (grouped position pos, row n = n0 + r) of this CTA: its partial
@@ -199,18 +181,22 @@ __device__ void base_issue(const FoldParams& p, uint32_t tmem, int nkb, uint8_t*
         if (ok) ok = warp_wait(&w_full[ws], (i / p.wstages) & 1, kWaitLimit, p.status, 27, p.diag);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t sw = smem_u32(wring + ws * kWTile);
-        const uint32_t sx = smem_u32(xring + xs * xs_bytes);
+        if (elect_one()) {
+            const uint32_t sw = smem_u32(wring + ws * kWTile);
+            const uint32_t sx = smem_u32(xring + xs * xs_bytes);
 #pragma unroll
-        for (int k16 = 0; k16 < 4; ++k16)
-            mma_bf16_ss(tmem, desc_sw128(sw + 32 * k16), desc_sw128(sx + 32 * k16), idb,
-                        (i > 0 || k16 > 0) ? 1u : 0u);
-        commit_elect(&w_empty[ws]);
-        commit_elect(&x_empty[xs]);
+            for (int k16 = 0; k16 < 4; ++k16)
+                mma_ss(tmem, desc_sw128(sw + 32 * k16), desc_sw128(sx + 32 * k16), idb, (i > 0 || k16 > 0) ? 1u : 0u);
+            mma_commit(&w_empty[ws]);
+            mma_commit(&x_empty[xs]);
+        }
+        __syncwarp();
     }
     __syncwarp();
-    if (ok) commit_elect(acc_full);
-    commit_elect(drain);                     // completes when every MMA of this warp has
+    if (elect_one()) {
+        if (ok) mma_commit(acc_full);
+        mma_commit(drain);                   // completes when every MMA of this warp has
+    }
 }
 
 // The sign issuer warp of a group: per 32-column K step j of block i, wait
@@ -261,30 +247,36 @@ __device__ void group_issue(const FoldParams& p, const FoldPlan& fp, uint32_t tm
                 tc_fence_after();
                 const uint32_t abuf = abase + j * 8 * ne;
                 const uint32_t soff = (static_cast<uint32_t>(xs) * xs_bytes >> 4) + 2u * j;
+                if (elect_one()) {
 #pragma unroll
-                for (int k = 0; k < kRegEntries; ++k)
-                    if (k < own) {
-                        const uint32_t blo = r_b[k] + soff;
-                        mma_e4m3_ts(r_d[k], abuf + r_a[k], (static_cast<uint64_t>(xdesc_hi) << 32) | blo, r_id[k]);
-                        mma_e4m3_ts(r_d[k], abuf + r_a[k], (static_cast<uint64_t>(xdesc_hi) << 32) | (blo + 4u), r_id[k]);
-                    }
-                commit_elect(&ge[j]);
-                if (j == 1) commit_elect(&x_empty[xs]);
+                    for (int k = 0; k < kRegEntries; ++k)
+                        if (k < own) {
+                            const uint32_t blo = r_b[k] + soff;
+                            mma_ts_f8(r_d[k], abuf + r_a[k], (static_cast<uint64_t>(xdesc_hi) << 32) | blo, r_id[k], 1u);
+                            mma_ts_f8(r_d[k], abuf + r_a[k], (static_cast<uint64_t>(xdesc_hi) << 32) | (blo + 4u), r_id[k], 1u);
+                        }
+                    mma_commit(&ge[j]);
+                    if (j == 1) mma_commit(&x_empty[xs]);
+                }
+                __syncwarp();
             } else if (work) {
                 tc_fence_after();
                 const uint32_t sxp = smem_u32(xring + xs * xs_bytes) + Mb * 128;
                 const uint32_t abuf = abase + j * 8 * ne;
-                for (int l = iss; l < ne; l += kGroupIss) {
-                    const int e = e0 + kIss * l;
-                    const uint32_t d = tmem + kSCol0 + fp.e_col[e];
-                    const uint32_t a = abuf + 8 * l;
-                    const uint32_t brow = sxp + fp.e_row[e] * 128 + 32 * j;
-                    const uint32_t id8 = idesc_e4m3(128, fp.e_n[e]);
-                    mma_e4m3_ts(d, a, desc_sw128(brow), id8);
-                    mma_e4m3_ts(d, a, desc_sw128(brow + 64), id8);
+                if (elect_one()) {
+                    for (int l = iss; l < ne; l += kGroupIss) {
+                        const int e = e0 + kIss * l;
+                        const uint32_t d = tmem + kSCol0 + fp.e_col[e];
+                        const uint32_t a = abuf + 8 * l;
+                        const uint32_t brow = sxp + fp.e_row[e] * 128 + 32 * j;
+                        const uint32_t id8 = idesc_e4m3(128, fp.e_n[e]);
+                        mma_ts_f8(d, a, desc_sw128(brow), id8, 1u);
+                        mma_ts_f8(d, a, desc_sw128(brow + 64), id8, 1u);
+                    }
+                    mma_commit(&ge[j]);
+                    if (j == 1) mma_commit(&x_empty[xs]);
                 }
-                commit_elect(&ge[j]);
-                if (j == 1) commit_elect(&x_empty[xs]);
+                __syncwarp();
             } else {
                 __syncwarp();
                 if (lane == 0) {
@@ -296,8 +288,10 @@ __device__ void group_issue(const FoldParams& p, const FoldPlan& fp, uint32_t tm
     }
     __syncwarp();
     if (work) {
-        if (ok) commit_elect(acc_full);
-        commit_elect(drain);
+        if (elect_one()) {
+            if (ok) mma_commit(acc_full);
+            mma_commit(drain);
+        }
     } else if (lane == 0) {
         if (ok) mbar_arrive(acc_full);
         mbar_arrive(drain);

@@ -74,22 +74,12 @@ __host__ __device__ constexpr uint32_t smem_bytes(int Mb) {
     return kStages * stage_bytes(Mb) + kBStages * 2048u + 1024u;
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-__device__ __forceinline__ void commit_elect(uint64_t* bar) {
-    asm volatile(
-        "{\n\t.reg .pred e;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
-            sm100::smem_u32(bar))
-        : "memory");
+// True in one lane of a converged warp (the lowest): the lane that issues the
+// MMAs and commits, so that each commit tracks that lane's MMAs.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t e;
+    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(e));
+    return e != 0;
 }
 __device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
     uint32_t a;
@@ -229,17 +219,20 @@ __global__ void __launch_bounds__(kThreads, 1) weff_decode_kernel(const __grid_c
             if (ok) ok = warp_wait(&built[s], (i / kStages) & 1, kWaitLimit, p.status, 45, p.diag);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t st = smem_u32(base + s * sbytes);
+            if (elect_one()) {               // one lane issues the block's MMAs and commit in a row
+                const uint32_t st = smem_u32(base + s * sbytes);
 #pragma unroll
-            for (int k16 = 0; k16 < 4; ++k16) {
-                const uint64_t bx = desc_sw128(st + 2 * kWTile + 32 * k16);
-                mma_bf16(tmem, desc_sw128(st + kWTile + 32 * k16), bx, idesc, (i > 0 || k16 > 0) ? 1u : 0u);
-                if (with_base) mma_bf16(tmem + 128, desc_sw128(st + 32 * k16), bx, idesc, (i > 0 || k16 > 0) ? 1u : 0u);
+                for (int k16 = 0; k16 < 4; ++k16) {
+                    const uint64_t bx = desc_sw128(st + 2 * kWTile + 32 * k16);
+                    mma_ss(tmem, desc_sw128(st + kWTile + 32 * k16), bx, idesc, (i > 0 || k16 > 0) ? 1u : 0u);
+                    if (with_base) mma_ss(tmem + 128, desc_sw128(st + 32 * k16), bx, idesc, (i > 0 || k16 > 0) ? 1u : 0u);
+                }
+                mma_commit(&empty[s]);
             }
-            commit_elect(&empty[s]);
+            __syncwarp();
         }
         __syncwarp();
-        commit_elect(&acc_full);             // completes when every MMA issued has (also after an error)
+        if (elect_one()) mma_commit(&acc_full);  // completes when every MMA issued has (also after an error)
         if (!ok && lane == 0) report(p.status, BD_ERR_TIMEOUT);
     } else {
         // ---------------- builders, then the epilogue ----------------
