@@ -114,14 +114,6 @@ __device__ __forceinline__ float pow2i(int e) {        // exact 2^e, e in [-126,
     return __int_as_float((127 + e) << 23);
 }
 
-// True in one lane of a converged warp (the lowest): the lane that issues the
-// warp's MMAs and commits, so that each commit tracks that lane's MMAs.
-__device__ __forceinline__ bool elect_one() {
-    uint32_t e;
-    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(e));
-    return e != 0;
-}
-
 // Output (grouped position pos, row n = n0 + r) of this CTA: its partial
 // tile in shared memory (cluster reduction), its K slice's partial in HBM
 // (ticket reduction), or y itself (one slice).

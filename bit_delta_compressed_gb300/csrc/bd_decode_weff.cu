@@ -74,13 +74,6 @@ __host__ __device__ constexpr uint32_t smem_bytes(int Mb) {
     return kStages * stage_bytes(Mb) + kBStages * 2048u + 1024u;
 }
 
-// True in one lane of a converged warp (the lowest): the lane that issues the
-// MMAs and commits, so that each commit tracks that lane's MMAs.
-__device__ __forceinline__ bool elect_one() {
-    uint32_t e;
-    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(e));
-    return e != 0;
-}
 __device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
     uint32_t a;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(saddr), "r"(rank));

@@ -188,6 +188,18 @@ __device__ __forceinline__ void mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint
         : "memory");
 }
 
+// True in one lane of a converged warp (the lowest).  A warp that waits as a
+// whole issues a run of MMAs and their commit inside one such branch -- each
+// commit then tracks that lane's MMAs; measured on the decode kernels, the
+// run costs far less issue time than an elect per MMA by the whole warp or a
+// plain lane-0 branch inside the warp's loop.  (An issuer whose whole loop,
+// waits included, runs in one lane needs neither.)
+__device__ __forceinline__ bool elect_one() {
+    uint32_t e;
+    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(e));
+    return e != 0;
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
