@@ -35,7 +35,7 @@
 //     from HBM by TMA;
 //   * 3, the base issuer: per block four bf16 MMAs (N = pad16(M)) of the W
 //     tile with X_c; the only consumer of the W ring;
-//   * four issuer groups of six warps.  An entry is one present variant
+//   * four issuer groups of five warps.  An entry is one present variant
 //     (its run of grouped positions, the 16-token chunks it touches and its
 //     rows of X_p; variant runs that share a chunk are separated by zero rows
 //     in X_p); entry e belongs to group e % 4, so the groups' loads differ by
@@ -44,10 +44,11 @@
 //     tiles in tensor memory (two buffers) -- one shift and one LOP3 per four
 //     weights: register j = ((w << (7 - j)) & 0x80808080) ^ 0xB8B8B8B8 holds
 //     columns j, j+8, j+16, j+24 of a 32-bit word -- and arrive on a named
-//     barrier; its two issuer warps then issue, per 32-column K step, two
-//     e4m3 sign products (hi, lo) per entry, the entries dealt to them
-//     alternately: the issue rate of a warp, not the tensor core, bounds a
-//     step.  Entries of different groups may add into the same accumulator
+//     barrier; its issuer warp then issues, per 32-column K step, two e4m3
+//     sign products (hi, lo) per entry: issue and hand-off latencies, not
+//     the tensor core, bound a step (with single-lane issue one issuer warp
+//     per group beats two: fewer warps contend for the schedulers and for
+//     tensor memory).  Entries of different groups may add into the same accumulator
 //     columns (each MMA's accumulation is atomic in the tensor pipe), so all
 //     sign columns are zeroed before the first sign product; at the end each
 //     group's expansion warps read a quarter of the columns of both
@@ -74,7 +75,7 @@ constexpr int kWMax = 4;                        // W_base ring stages (runtime: 
 constexpr int kXMax = 2;                        // activation ring stages (runtime: 1 or 2)
 constexpr int kBStages = 2;                     // bits ring stages, two 64-column blocks each
 constexpr int kIss = kFoldIssuers;             // issuer groups
-constexpr int kGroupIss = 2;                    // issuer warps per group (entries dealt alternately)
+constexpr int kGroupIss = 1;                    // issuer warps per group (entries dealt in turn)
 constexpr int kGroupWarps = 4 + kGroupIss;      // 4 expansion warps (one per lane quarter) + the issuers
 constexpr int kBaseWarp = 3;                    // the base-product issuer
 constexpr int kFirstGroup = 4;                  // warps 0, 1, 2: W, activation and bits producers
